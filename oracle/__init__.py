@@ -1,0 +1,14 @@
+"""Float64 CPU oracle (test infrastructure only; see sink_attention.py).
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg import
+this package.  The CUDA library never does, and this package never imports
+the CUDA library.
+"""
+from .sink_attention import (  # noqa: F401
+    attend_rows,
+    decode,
+    gather_paged_kv,
+    online_split_merge,
+    prefill,
+    sink_softmax_rows,
+)

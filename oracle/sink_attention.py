@@ -1,0 +1,267 @@
+"""Float64 CPU oracle for grouped-query attention with a per-head sink logit.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may call it.  It shares no code,
+table or helper with the CUDA library.
+
+Source: Perplexity, "GPT-OSS on day 0" (2025-08-08).
+  * Model overview, attention bullet: the attention is grouped-query attention
+    (several query heads read one key/value head) and every attention head
+    owns one trained sink parameter that takes part in the softmax.
+  * Section "Sink Attention" (under "Kernels for GPT-OSS"):
+      - first formula: the attention weights are a softmax of the scaled
+        query-key products together with the head's sink, and the result is
+        multiplied by V;
+      - second formula: softmax written with the row maximum subtracted;
+      - closing paragraph: the online form keeps a running maximum m and a
+        running scale d; starting m at the head's sink (with d = 1) folds the
+        sink into the normaliser once, and when the key/value length is split
+        into chunks only the first chunk may be seeded with it.
+
+Readings taken where the pages leave a step open (each also listed in the
+design notes of this repository):
+  * The sink is one extra logit per query head in the softmax normaliser; it
+    has no value vector, so its column is dropped before multiplying by V.
+    (Adding the sink to every logit would cancel inside the softmax and could
+    not be what "initialise m to the sink, d to 1" implements.)
+  * The sink is not multiplied by the softmax scale; it is already a logit.
+  * Query head h reads key/value head h // (Hq / Hkv).
+  * Prefill is causal with query length equal to key length: query i of a
+    sequence sees keys 0..i of the same sequence.
+  * Decode: the single query of sequence b sees all seqlens[b] cached keys.
+  * Degenerate rows: with no key and sink = -inf the output is defined as 0;
+    sink = +inf is taken as its limit (output 0).
+
+Precision: every quantity is float64; bf16 inputs are upcast exactly.
+
+Parity pins (tests/test_oracle_pins.py): every public function here is pinned
+against something other than itself -- brute force at 50 digits, a library
+attention routine, closed forms, hand-derived golden values, and invariants
+(normalisation, split invariance, GQA = repeated-KV MHA, page permutation
+invariance).  No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "sink_softmax_rows",
+    "attend_rows",
+    "prefill",
+    "decode",
+    "gather_paged_kv",
+    "online_split_merge",
+]
+
+# Rows of the score matrix computed at once, only to bound memory (the result
+# does not depend on it: each row is an independent softmax).
+_ROW_BLOCK = 512
+
+
+def _as_f64(x) -> np.ndarray:
+    """Upcast a numpy array or a (CPU) torch tensor exactly to float64."""
+    if hasattr(x, "detach"):  # torch tensor; bf16 -> f32 -> f64 is exact
+        x = x.detach().to("cpu")
+        if str(x.dtype) == "torch.bfloat16":
+            x = x.float()
+        x = x.numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _as_int(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.asarray(x, dtype=np.int64)
+
+
+def sink_softmax_rows(s: np.ndarray, sink: float):
+    """Softmax of each row of ``s`` extended by one extra logit ``sink``.
+
+    GPT-OSS on day 0, "Sink Attention": softmax of the scaled products with the
+    head's sink, evaluated with the maximum subtracted (second formula).
+
+    s    : [r, n] float64 logits (masked entries are -inf)
+    sink : scalar logit of the head (may be +-inf)
+    Returns (p [r, n], p_sink [r]) with p.sum(1) + p_sink == 1 for every row
+    that has at least one finite logit.  A row with no finite logit and
+    sink = -inf has no defined softmax: it returns all zeros (output 0).
+    sink = +inf gives p = 0, p_sink = 1 (the limit).
+    """
+    s = np.asarray(s, dtype=np.float64)
+    r, n = s.shape
+    if sink == math.inf:
+        return np.zeros_like(s), np.ones(r)
+    row_max = s.max(axis=1) if n > 0 else np.full(r, -math.inf)
+    m = np.maximum(row_max, sink)  # the subtracted maximum includes the sink
+    empty = m == -math.inf
+    m_safe = np.where(empty, 0.0, m)
+    e = np.exp(s - m_safe[:, None])
+    e_sink = np.exp(sink - m_safe)
+    z = e.sum(axis=1) + e_sink
+    z_safe = np.where(empty, 1.0, z)
+    p = e / z_safe[:, None]
+    p_sink = np.where(empty, 0.0, e_sink / z_safe)
+    p[empty] = 0.0
+    return p, p_sink
+
+
+def attend_rows(s: np.ndarray, sink: float, v: np.ndarray):
+    """Sink attention for a block of query rows sharing one key/value set.
+
+    s : [r, n] scaled logits (masked = -inf), v : [n, D].
+    Returns (out [r, D], lse [r]) where out = p @ v (the sink column is
+    dropped: it has no value vector) and lse = log(sum_j e^s_j + e^sink), the
+    natural-log normaliser including the sink (-inf for an empty row).
+    """
+    p, p_sink = sink_softmax_rows(s, sink)
+    out = p @ np.asarray(v, dtype=np.float64)
+    n = s.shape[1]
+    row_max = s.max(axis=1) if n > 0 else np.full(s.shape[0], -math.inf)
+    m = np.maximum(row_max, sink)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        m_safe = np.where(np.isfinite(m), m, 0.0)
+        z = np.exp(s - m_safe[:, None]).sum(axis=1) + np.exp(sink - m_safe)
+        lse = np.where(np.isfinite(m), m_safe + np.log(z), m)
+    return out, lse
+
+
+def prefill(q, k, v, sinks, cu_seqlens, scale: float):
+    """Causal variable-length prefill (definition, float64).
+
+    q : [T, Hq, D], k, v : [T, Hkv, D] packed over sequences,
+    sinks : [Hq], cu_seqlens : [B+1] (cu[0] = 0, non-decreasing, cu[B] = T).
+    For sequence b, local query i and head h (kv head g = h // (Hq/Hkv)):
+        s_j = scale * <q[i,h], k[j,g]>   for j = 0..i
+        out[i,h] = softmax([s_0..s_i, sinks[h]]) restricted to j, times v[j,g].
+    Returns (out [T, Hq, D], lse [T, Hq]).
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    sinks = _as_f64(sinks)
+    cu = _as_int(cu_seqlens)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    assert hq % hkv == 0, "query heads must be a multiple of kv heads"
+    group = hq // hkv
+    out = np.zeros((T, hq, d))
+    lse = np.full((T, hq), -math.inf)
+    for b in range(len(cu) - 1):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        L = t1 - t0
+        if L == 0:
+            continue
+        for h in range(hq):
+            g = h // group
+            kk = k[t0:t1, g, :]
+            vv = v[t0:t1, g, :]
+            for r0 in range(0, L, _ROW_BLOCK):
+                r1 = min(L, r0 + _ROW_BLOCK)
+                # keys beyond r1-1 are masked for every row of this block
+                s = scale * (q[t0 + r0:t0 + r1, h, :] @ kk[:r1].T)
+                rows = np.arange(r0, r1)[:, None]
+                cols = np.arange(r1)[None, :]
+                s = np.where(cols <= rows, s, -math.inf)
+                o, l = attend_rows(s, float(sinks[h]), vv[:r1])
+                out[t0 + r0:t0 + r1, h, :] = o
+                lse[t0 + r0:t0 + r1, h] = l
+    return out, lse
+
+
+def gather_paged_kv(pages, page_table_row, length: int, page_size: int):
+    """Contiguous [length, Hkv, D] view of one sequence's paged cache.
+
+    pages : [num_pages, Hkv, page_size, D]; token j of the sequence lives at
+    pages[page_table_row[j // page_size], :, j % page_size, :].
+    """
+    pages = _as_f64(pages)
+    row = _as_int(page_table_row)
+    n_pages = (length + page_size - 1) // page_size
+    hkv, d = pages.shape[1], pages.shape[3]
+    out = np.zeros((n_pages * page_size, hkv, d))
+    for p in range(n_pages):
+        out[p * page_size:(p + 1) * page_size] = pages[int(row[p])].transpose(1, 0, 2)
+    return out[:length]
+
+
+def decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: float,
+           page_size: int = 16):
+    """One query per sequence against a paged KV cache (definition, float64).
+
+    q : [B, Hq, D]; k_pages, v_pages : [num_pages, Hkv, page_size, D];
+    page_table : [B, stride]; seqlens : [B].  The query of sequence b attends
+    to all seqlens[b] cached keys (no mask).  Returns (out [B,Hq,D], lse [B,Hq]).
+    """
+    q = _as_f64(q)
+    sinks = _as_f64(sinks)
+    table = _as_int(page_table)
+    lens = _as_int(seqlens)
+    B, hq, d = q.shape
+    kp = _as_f64(k_pages)
+    vp = _as_f64(v_pages)
+    hkv = kp.shape[1]
+    group = hq // hkv
+    out = np.zeros((B, hq, d))
+    lse = np.full((B, hq), -math.inf)
+    for b in range(B):
+        L = int(lens[b])
+        kk = gather_paged_kv(kp, table[b], L, page_size)
+        vv = gather_paged_kv(vp, table[b], L, page_size)
+        for h in range(hq):
+            g = h // group
+            s = scale * (q[b, h][None, :] @ kk[:, g, :].T)
+            o, l = attend_rows(s, float(sinks[h]), vv[:, g, :])
+            out[b, h] = o[0]
+            lse[b, h] = l[0]
+    return out, lse
+
+
+def online_split_merge(s_row, sink: float, v, cuts):
+    """The pages' online algorithm for one query row, split along key length.
+
+    GPT-OSS on day 0, "Sink Attention", closing paragraph: each chunk keeps a
+    running maximum m and scale d (plus the weighted value sum).  The first
+    chunk starts from m = sink, d = 1, which counts the sink once; every other
+    chunk starts from the plain state m = -inf, d = 1.  Partial states are then
+    combined by rescaling to the common maximum (the pages only imply this
+    step; it is the standard combination of softmax partial sums).
+
+    s_row : [n] logits, v : [n, D], cuts : sorted chunk boundaries inside
+    (0, n).  Pure Python loops: small inputs only.  Returns out [D].
+    """
+    s_row = [float(x) for x in s_row]
+    v = _as_f64(v)
+    n, d = v.shape
+    bounds = [0] + [int(c) for c in cuts] + [n]
+    states = []
+    for c in range(len(bounds) - 1):
+        m, dd = (sink, 1.0) if c == 0 else (-math.inf, 1.0)
+        acc = np.zeros(d)
+        for j in range(bounds[c], bounds[c + 1]):
+            x = s_row[j]
+            if x == -math.inf:
+                continue  # e^-inf = 0 adds nothing
+            m_new = max(m, x)
+            alpha = math.exp(m - m_new) if m != -math.inf else 0.0
+            w = math.exp(x - m_new)
+            dd = dd * alpha + w
+            acc = acc * alpha + w * v[j]
+            m = m_new
+        if m == -math.inf:
+            dd = 0.0  # a chunk that saw nothing holds no mass
+        states.append((m, dd, acc))
+    big_m = max(st[0] for st in states)
+    if big_m == -math.inf:
+        return np.zeros(d)
+    if big_m == math.inf:
+        return np.zeros(d)
+    total_d = 0.0
+    total = np.zeros(d)
+    for m, dd, acc in states:
+        if m == -math.inf:
+            continue
+        w = math.exp(m - big_m)
+        total_d += dd * w
+        total += acc * w
+    return total / total_d
