@@ -1,0 +1,197 @@
+"""ctypes binding of libsink_attn.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (declared in
+include/sink_attn.h).  Tensors are torch tensors on a CUDA device; torch only
+provides the device memory and the current stream.  Nothing here computes any
+part of the attention: if the library is missing the calls raise, there is no
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_LIB = None
+
+OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+                4: "device-side wait timed out", 5: "out of device memory"}
+OUT_BF16 = 0
+OUT_F32 = 1
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+EXPORTS = {
+    "sink_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P]),
+    "sink_attn_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P,
+                              _P, _SZ, _P]),
+    "sink_attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "sink_attn_decode_max_splits": (_I, [_I, _I, _I, _I, _I]),
+    "sink_attn_status_string": (ctypes.c_char_p, [_I]),
+    "sink_attn_get_device_error": (_I, [_P]),
+    "sink_attn_version": (_I, []),
+}
+
+
+class SinkAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, 'unknown status')} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with gqa_attention_head_sink_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in EXPORTS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == library_path():
+        _LIB = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise SinkAttnError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def sink_attn_status_string(status: int) -> str:
+    return load().sink_attn_status_string(int(status)).decode()
+
+
+def sink_attn_version() -> int:
+    return load().sink_attn_version()
+
+
+def sink_attn_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) a recorded device timeout."""
+    return load().sink_attn_get_device_error(_stream_ptr(stream))
+
+
+def sink_attn_prefill(q, k, v, sinks, cu_seqlens, scale: float, out=None, out_dtype=torch.float32,
+                      lse=None, max_seqlen: Optional[int] = None, stream=None):
+    """Causal varlen prefill.  q [T,Hq,64], k/v [T,Hkv,64] bf16; sinks [Hq] fp32;
+    cu_seqlens [B+1] int32.  Returns out [T,Hq,64] (bf16 or fp32).  Pass
+    ``max_seqlen`` to avoid a device->host read of the lengths."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(sinks, "sinks", torch.float32, 1)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if k.shape != (T, hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [T, Hkv, D] with the same T and D as q")
+    if sinks.shape[0] != hq:
+        raise ValueError("sinks must have one entry per query head")
+    B = cu_seqlens.shape[0] - 1
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 0
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=out_dtype, device=q.device)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    _need(out, "out", out.dtype, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    st = load().sink_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), B, T, int(max_seqlen),
+                                  hq, hkv, d, float(scale), _ptr(out),
+                                  OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse),
+                                  _stream_ptr(stream))
+    _check(st, "sink_attn_prefill")
+    return out
+
+
+def sink_attn_decode_workspace_bytes(batch: int, max_seqlen: int, num_q_heads: int, num_kv_heads: int,
+                                     head_dim: int = 64, page_size: int = 16, num_splits: int = 0) -> int:
+    n = load().sink_attn_decode_workspace_bytes(batch, max_seqlen, num_q_heads, num_kv_heads, head_dim,
+                                                page_size, num_splits)
+    if n == ctypes.c_size_t(-1).value:
+        raise SinkAttnError(1, "sink_attn_decode_workspace_bytes")
+    return n
+
+
+def sink_attn_decode_max_splits(batch: int, max_seqlen: int, num_kv_heads: int, page_size: int = 16,
+                                num_splits: int = 0) -> int:
+    return load().sink_attn_decode_max_splits(batch, max_seqlen, num_kv_heads, page_size, num_splits)
+
+
+def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: float, num_splits: int = 0,
+                     out=None, out_dtype=torch.float32, lse=None, max_seqlen: Optional[int] = None,
+                     workspace=None, stream=None):
+    """Split-KV paged decode.  q [B,Hq,64] bf16; k_pages/v_pages
+    [num_pages,Hkv,16,64] bf16; page_table [B,stride] int32; seqlens [B]
+    int32; sinks [Hq] fp32.  ``workspace``: optional uint8 CUDA tensor of at
+    least sink_attn_decode_workspace_bytes(...) bytes (else the library
+    allocates in stream order).  Returns out [B,Hq,64]."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    B, hq, d = q.shape
+    num_pages, hkv, page_size, d2 = k_pages.shape
+    if v_pages.shape != k_pages.shape or d2 != d:
+        raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
+    if page_table.shape[0] != B or seqlens.shape[0] != B:
+        raise ValueError("page_table and seqlens need one row per sequence")
+    if max_seqlen is None:
+        max_seqlen = int(seqlens.max().item()) if B > 0 else 0
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    _need(out, "out", out.dtype, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = load().sink_attn_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), page_table.shape[1],
+                                 _ptr(seqlens), B, int(max_seqlen), num_pages, _ptr(sinks), hq, hkv, d, page_size,
+                                 float(scale), int(num_splits), _ptr(out),
+                                 OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse), ws_ptr,
+                                 ws_bytes, _stream_ptr(stream))
+    _check(st, "sink_attn_decode")
+    return out

@@ -1,0 +1,339 @@
+// C ABI of the sink-attention library: argument validation, planning, TMA
+// tensor-map encoding, workspace handling and kernel launches.  The entry
+// points are declared (and documented) in include/sink_attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/sink_attn.h"
+#include "decode.h"
+#include "prefill.h"
+
+namespace sa {
+
+// Timeouts recorded by bounded device-side waits (see common.cuh).
+__device__ unsigned g_error_word;
+
+namespace {
+
+constexpr int kHeadDim = 64;
+constexpr int kPageSize = 16;
+constexpr int kMaxSplits = 256;
+constexpr int kMaxGroupDecode = 16;
+constexpr int kMaxDevices = 64;
+// Chunk sizing for num_splits == 0: aim for about this many CTAs in the
+// chunk grid (8 per SM of a 152-SM GB300) with 16..128 pages per chunk.
+constexpr long long kDecodeTargetCtas = 152 * 8;
+constexpr int kMinSplitPages = 16;
+constexpr int kMaxSplitPages = 128;
+
+std::mutex g_mutex;
+unsigned* g_err_ptr[kMaxDevices] = {};
+bool g_prefill_attr_set[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("SINK_ATTN_WAIT_LIMIT_MS");
+    long long ms = s ? std::atoll(s) : 4000;
+    if (ms <= 0) ms = 4000;
+    return (uint64_t)ms * 1000000ull;
+  }();
+  return v;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return SINK_ATTN_ERR_UNSUPPORTED;
+  return SINK_ATTN_OK;
+}
+
+int error_word(int dev, unsigned** out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return SINK_ATTN_OK;
+}
+
+int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return SINK_ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return SINK_ATTN_OK;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, 64] view (128-byte rows) with
+// boxes of `box_rows` x 64 and the 128-byte swizzle.
+int encode_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int st = get_encoder(&enc);
+  if (st) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_stride_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)kHeadDim, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
+}
+
+// 3-D bf16 tensor map over a packed [tokens, heads, 64] tensor, boxes of
+// 128 tokens x 1 head x 64 dims (one 16 KiB tile of one head), 128-byte swizzle.
+int encode_tokens_heads(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int st = get_encoder(&enc);
+  if (st) return st;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kPrefillTileRows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
+}
+
+struct DecodePlan {
+  int max_splits;
+  int split_pages;
+  bool direct;
+  size_t ws_bytes;
+};
+
+bool plan_decode(int batch, int max_seqlen, int num_q_heads, int num_kv_heads, int num_splits, DecodePlan* pl) {
+  if (batch < 0 || max_seqlen < 0 || num_kv_heads <= 0 || num_q_heads <= 0) return false;
+  if (num_splits < 0 || num_splits > kMaxSplits) return false;
+  const long long max_pages = ((long long)max_seqlen + kPageSize - 1) / kPageSize;
+  int split_pages = kMaxSplitPages;
+  int max_splits;
+  if (num_splits > 0) {
+    max_splits = (int)std::max(1LL, std::min<long long>(num_splits, max_pages));
+  } else {
+    long long sp = ((long long)batch * num_kv_heads * max_pages + kDecodeTargetCtas - 1) / kDecodeTargetCtas;
+    sp = std::min<long long>(kMaxSplitPages, std::max<long long>(kMinSplitPages, sp));
+    if ((max_pages + sp - 1) / sp > kMaxSplits) sp = (max_pages + kMaxSplits - 1) / kMaxSplits;
+    split_pages = (int)sp;
+    max_splits = (int)std::max(1LL, (max_pages + sp - 1) / sp);
+  }
+  pl->max_splits = max_splits;
+  pl->split_pages = split_pages;
+  pl->direct = max_splits == 1;
+  if (pl->direct) {
+    pl->ws_bytes = 0;
+  } else {
+    const size_t slots = (size_t)batch * num_q_heads * max_splits;
+    const size_t o_bytes = (slots * kHeadDim * 4 + 255) / 256 * 256;
+    pl->ws_bytes = o_bytes + slots * 2 * 4;
+  }
+  return true;
+}
+
+}  // namespace
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" {
+
+int sink_attn_version(void) { return 100; }
+
+const char* sink_attn_status_string(int status) {
+  switch (status) {
+    case SINK_ATTN_OK: return "ok";
+    case SINK_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case SINK_ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SINK_ATTN_ERR_CUDA: return "CUDA error";
+    case SINK_ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    case SINK_ATTN_ERR_NO_MEMORY: return "out of device memory";
+    default: return "unknown status";
+  }
+}
+
+int sink_attn_get_device_error(void* stream) {
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  unsigned* w;
+  if ((st = error_word(dev, &w))) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+    return SINK_ATTN_ERR_TIMEOUT;
+  }
+  return SINK_ATTN_OK;
+}
+
+int sink_attn_decode_max_splits(int batch, int max_seqlen, int num_kv_heads, int page_size, int num_splits) {
+  if (page_size != kPageSize) return 0;
+  DecodePlan pl;
+  if (!plan_decode(batch, max_seqlen, num_kv_heads, num_kv_heads, num_splits, &pl)) return 0;
+  return pl.max_splits;
+}
+
+size_t sink_attn_decode_workspace_bytes(int batch, int max_seqlen, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int page_size, int num_splits) {
+  if (head_dim != kHeadDim || page_size != kPageSize) return (size_t)-1;
+  DecodePlan pl;
+  if (!plan_decode(batch, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl)) return (size_t)-1;
+  return pl.ws_bytes;
+}
+
+int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                     int page_table_stride, const int32_t* seqlens, int batch, int max_seqlen, int num_pages,
+                     const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                     float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  // ---- validation (nothing is enqueued on failure)
+  if (batch < 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0) return SINK_ATTN_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return SINK_ATTN_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > kMaxSplits) return SINK_ATTN_ERR_INVALID_ARG;
+  if (out_dtype != SINK_ATTN_OUT_BF16 && out_dtype != SINK_ATTN_OUT_F32) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return SINK_ATTN_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || page_size != kPageSize) return SINK_ATTN_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads > kMaxGroupDecode) return SINK_ATTN_ERR_UNSUPPORTED;
+  if (batch == 0) return SINK_ATTN_OK;
+  if (!q || !k_pages || !v_pages || !page_table || !seqlens || !sinks || !out) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(page_table) ||
+      !aligned16(seqlens) || !aligned16(sinks) || !aligned16(out) || (lse && !aligned16(lse)))
+    return SINK_ATTN_ERR_INVALID_ARG;
+  if (num_pages <= 0 || page_table_stride <= 0) return SINK_ATTN_ERR_INVALID_ARG;
+  if ((long long)page_table_stride * kPageSize < max_seqlen) return SINK_ATTN_ERR_INVALID_ARG;
+  if (batch > 65535 || num_kv_heads > 65535) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)num_pages * num_kv_heads * kPageSize >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
+  DecodePlan pl;
+  if (!plan_decode(batch, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl)) return SINK_ATTN_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SINK_ATTN_ERR_INVALID_ARG;
+  if (workspace && workspace_bytes < pl.ws_bytes) return SINK_ATTN_ERR_INVALID_ARG;
+
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  unsigned* err;
+  if ((st = error_word(dev, &err))) return st;
+  const uint64_t rows = (uint64_t)num_pages * num_kv_heads * kPageSize;
+  CUtensorMap kmap, vmap;
+  if ((st = encode_rows64(&kmap, k_pages, rows, kHeadDim * 2, kPageSize))) return st;
+  if ((st = encode_rows64(&vmap, v_pages, rows, kHeadDim * 2, kPageSize))) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  bool owned = false;
+  if (pl.ws_bytes && !ws) {
+    if (cudaMallocAsync(&ws, pl.ws_bytes, s) != cudaSuccess) {
+      cudaGetLastError();
+      return SINK_ATTN_ERR_NO_MEMORY;
+    }
+    owned = true;
+  }
+  DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.page_table = page_table;
+  p.seqlens = seqlens;
+  p.sinks = sinks;
+  p.out = out;
+  p.lse = lse;
+  if (pl.ws_bytes) {
+    const size_t slots = (size_t)batch * num_q_heads * pl.max_splits;
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_md = reinterpret_cast<float*>(static_cast<char*>(ws) + (slots * kHeadDim * 4 + 255) / 256 * 256);
+  }
+  p.err = err;
+  p.batch = batch;
+  p.hq = num_q_heads;
+  p.hkv = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.stride = page_table_stride;
+  p.num_splits = num_splits;
+  p.split_pages = pl.split_pages;
+  p.max_splits = pl.max_splits;
+  p.direct = pl.direct ? 1 : 0;
+  p.out_f32 = out_dtype == SINK_ATTN_OUT_F32;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_ns();
+  cudaError_t e = launch_decode(kmap, vmap, p, s);
+  if (owned) cudaFreeAsync(ws, s);
+  return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
+}
+
+int sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks, const int32_t* cu_seqlens,
+                      int batch, int total_tokens, int max_seqlen, int num_q_heads, int num_kv_heads,
+                      int head_dim, float scale, void* out, int out_dtype, float* lse, void* stream) {
+  if (batch < 0 || total_tokens < 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+    return SINK_ATTN_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return SINK_ATTN_ERR_INVALID_ARG;
+  if (out_dtype != SINK_ATTN_OUT_BF16 && out_dtype != SINK_ATTN_OUT_F32) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return SINK_ATTN_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return SINK_ATTN_ERR_UNSUPPORTED;
+  if (max_seqlen > total_tokens) return SINK_ATTN_ERR_INVALID_ARG;
+  if (batch == 0 || total_tokens == 0) return SINK_ATTN_OK;
+  if (!q || !k || !v || !sinks || !cu_seqlens || !out) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(sinks) || !aligned16(cu_seqlens) ||
+      !aligned16(out) || (lse && !aligned16(lse)))
+    return SINK_ATTN_ERR_INVALID_ARG;
+  if (batch > kPrefillMaxBatch || max_seqlen >= (1 << 24)) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)total_tokens * num_q_heads >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
+
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  unsigned* err;
+  if ((st = error_word(dev, &err))) return st;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_prefill_attr_set[dev]) {
+      if (prefill_configure() != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+      g_prefill_attr_set[dev] = true;
+    }
+  }
+  CUtensorMap qmap, kmap, vmap;
+  if ((st = encode_tokens_heads(&qmap, q, total_tokens, num_q_heads))) return st;
+  if ((st = encode_tokens_heads(&kmap, k, total_tokens, num_kv_heads))) return st;
+  if ((st = encode_tokens_heads(&vmap, v, total_tokens, num_kv_heads))) return st;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+
+  PrefillParams p{};
+  p.cu_seqlens = cu_seqlens;
+  p.sinks = sinks;
+  p.out = out;
+  p.lse = lse;
+  p.err = err;
+  p.batch = batch;
+  p.total_tokens = total_tokens;
+  p.hq = num_q_heads;
+  p.hkv = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.max_qblocks = (max_seqlen + kPrefillTileRows - 1) / kPrefillTileRows;
+  p.out_f32 = out_dtype == SINK_ATTN_OUT_F32;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_ns();
+  cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,397 @@
+// Split-KV paged decode with a per-head sink logit (sm_103a).
+//
+// Method: Perplexity, "GPT-OSS on day 0", section "Sink Attention".  The key
+// length of each sequence is cut into chunks of whole pages; every chunk keeps
+// the online-softmax state (running max m, running scale d, weighted value sum)
+// and only the first chunk's state starts from the head's sink (m = sink,
+// d = 1).  A second kernel combines the chunks' (m, d, acc) triples.
+//
+// Work decomposition: one CTA per (chunk, kv head, sequence).  The CTA holds
+// the G = Hq/Hkv query heads that share the kv head, so every page of K/V is
+// read from HBM exactly once.  Roles:
+//   * warp 4 (producer): reads the page-table entries of the chunk and streams
+//     each (page, kv head) slab -- 16 tokens x 64 dims x bf16 = 2 KiB of K and
+//     2 KiB of V, contiguous in the [page, kv_head, slot, dim] layout -- into a
+//     ring of shared-memory stages with 2-D TMA copies (128-byte swizzle), one
+//     mbarrier per stage completing on the transferred bytes;
+//   * warps 0..3 (consumers): warp w takes pages w, w+4, ...  For one page it
+//     computes S = Q K^T (16 rows = query heads of the group, padded; 16
+//     tokens) and O += P V with warp-level bf16 MMAs (m16n8k16, fp32
+//     accumulate), the online softmax in registers, and releases the stage as
+//     soon as K and V are in registers.
+// The four warps' states are merged in shared memory; with a single chunk
+// the CTA writes the normalised output directly, otherwise its partial state.
+//
+// Fragment layouts (m16n8k16): lane = 4*r + qd.  The head dimension is used in
+// a permuted order that is the same for Q and K (a dot product does not care),
+// chosen so that each lane reads 32 contiguous bytes of a K row; the output
+// dimension is permuted so that each lane reads 16 contiguous bytes of a V row
+// and ends up owning 16 contiguous output dimensions.  With the 128-byte TMA
+// swizzle (16-byte chunk c of row t stored at chunk c ^ (t % 8)) every shared
+// load below is free of bank conflicts.
+#include "common.cuh"
+#include "decode.h"
+
+namespace sa {
+
+namespace {
+
+constexpr int kD = 64;
+constexpr int kPage = 16;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 8;
+constexpr int kSlabBytes = kPage * kD * 2;      // 2048
+constexpr int kStageBytes = 2 * kSlabBytes;     // K + V
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kRows = 16;                       // MMA rows = query heads per group (padded)
+// merge scratch per warp: m[16], d[16], o[16][64]
+constexpr int kScratchFloatsPerWarp = kRows * 2 + kRows * kD;
+static_assert(kConsumerWarps * kScratchFloatsPerWarp * 4 <= kRingBytes, "merge scratch aliases the ring");
+
+__device__ __forceinline__ void chunk_range(const DecodeParams& p, int L, int s, int& n, int& pg0, int& pg1) {
+  const int npages = (L + kPage - 1) / kPage;
+  n = decode_num_chunks(npages, p.num_splits, p.split_pages, p.max_splits);
+  const int chunk = npages > 0 ? (npages + n - 1) / n : 0;
+  pg0 = s * chunk;
+  pg1 = min(npages, pg0 + chunk);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                const __grid_constant__ CUtensorMap vmap,
+                                                                const DecodeParams p) {
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // a length beyond the page-table row is clamped: never read past the row
+  const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
+  int n, pg0, pg1;
+  chunk_range(p, L, s, n, pg0, pg1);
+  if (s >= n) return;
+  const int count = max(0, pg1 - pg0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRingBytes);
+  uint64_t* empty = full + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+    }
+    const uint64_t policy = l2_policy_evict_first();  // K/V are read once
+    const int32_t* row = p.page_table + (size_t)b * p.stride;
+    for (int base = 0; base < count; base += 32) {
+      const int mine = base + lane;
+      const int page_l = mine < count ? __ldg(row + pg0 + mine) : 0;
+      const int m = min(32, count - base);
+      for (int j = 0; j < m; ++j) {
+        const int page = __shfl_sync(0xffffffffu, page_l, j);
+        if (lane == 0) {
+          const int i = base + j, st = i % kStages;
+          bool ok = true;
+          if (i >= kStages) ok = mbar_wait(&empty[st], ((i / kStages) - 1) & 1, p.err, kErrDecodeEmpty, p.wait_limit_ns);
+          if (!ok || *abort_flag) {
+            *abort_flag = 1;
+          } else {
+            uint8_t* dst = smem + st * kStageBytes;
+            const int y = (page * p.hkv + g) * kPage;
+            mbar_arrive_expect_tx(&full[st], kStageBytes);
+            tma_load_2d_hint(dst, &kmap, &full[st], 0, y, policy);
+            tma_load_2d_hint(dst + kSlabBytes, &vmap, &full[st], 0, y, policy);
+          }
+        }
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      }
+      if (*abort_flag) break;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int r = lane >> 2, qd = lane & 3;
+  const int G = p.group;
+  const int h_r = g * G + r, h_r8 = g * G + r + 8;
+  const bool row_ok = r < G, row8_ok = r + 8 < G;
+
+  // Query fragments: row r holds dims [16qd, 16qd+16) of head h_r.
+  uint32_t qa[4][4];
+  {
+    uint4 lo_r = make_uint4(0, 0, 0, 0), hi_r = lo_r, lo_r8 = lo_r, hi_r8 = lo_r;
+    const uint4* qb = reinterpret_cast<const uint4*>(p.q + (size_t)b * p.hq * kD);
+    if (row_ok) {
+      lo_r = __ldg(qb + (h_r * kD + 16 * qd) / 8);
+      hi_r = __ldg(qb + (h_r * kD + 16 * qd) / 8 + 1);
+    }
+    if (row8_ok) {
+      lo_r8 = __ldg(qb + (h_r8 * kD + 16 * qd) / 8);
+      hi_r8 = __ldg(qb + (h_r8 * kD + 16 * qd) / 8 + 1);
+    }
+    const uint32_t wr[8] = {lo_r.x, lo_r.y, lo_r.z, lo_r.w, hi_r.x, hi_r.y, hi_r.z, hi_r.w};
+    const uint32_t wr8[8] = {lo_r8.x, lo_r8.y, lo_r8.z, lo_r8.w, hi_r8.x, hi_r8.y, hi_r8.z, hi_r8.w};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      qa[kk][0] = wr[2 * kk];
+      qa[kk][1] = wr8[2 * kk];
+      qa[kk][2] = wr[2 * kk + 1];
+      qa[kk][3] = wr8[2 * kk + 1];
+    }
+  }
+
+  // Online-softmax state for rows r and r+8 (log2 domain).  Only the first
+  // chunk's first warp starts from the sink: m = sink * log2(e), d = 1.
+  float m_r = -INFINITY, m_r8 = -INFINITY, d_r = 0.f, d_r8 = 0.f;
+  if (s == 0 && warp == 0) {
+    m_r = row_ok ? __ldg(p.sinks + h_r) * kLog2e : -INFINITY;
+    m_r8 = row8_ok ? __ldg(p.sinks + h_r8) * kLog2e : -INFINITY;
+    if (qd == 0) {
+      d_r = 1.f;
+      d_r8 = 1.f;
+    }
+  }
+  float o[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+  const float sl2 = p.scale_log2;
+  for (int i = warp; i < count; i += kConsumerWarps) {
+    const int st = i % kStages;
+    if (!mbar_wait(&full[st], (i / kStages) & 1, p.err, kErrDecodeFull, p.wait_limit_ns)) {
+      *abort_flag = 1;
+      break;
+    }
+    if (*abort_flag) break;
+    const uint8_t* ks = smem + st * kStageBytes;
+    const uint8_t* vs = ks + kSlabBytes;
+    // K rows t = nt*8 + r, 16-byte chunks 2qd and 2qd+1 (swizzled by t % 8 = r)
+    uint4 k0a = lds128(ks + r * 128 + (((2 * qd) ^ r) << 4));
+    uint4 k0b = lds128(ks + r * 128 + (((2 * qd + 1) ^ r) << 4));
+    uint4 k1a = lds128(ks + (8 + r) * 128 + (((2 * qd) ^ r) << 4));
+    uint4 k1b = lds128(ks + (8 + r) * 128 + (((2 * qd + 1) ^ r) << 4));
+    // V rows 2qd, 2qd+1, 2qd+8, 2qd+9, chunk r (dims 8r..8r+7)
+    const int t0 = 2 * qd, t1 = 2 * qd + 1;
+    uint4 va = lds128(vs + t0 * 128 + ((r ^ t0) << 4));
+    uint4 vb = lds128(vs + t1 * 128 + ((r ^ t1) << 4));
+    uint4 vc = lds128(vs + (t0 + 8) * 128 + ((r ^ t0) << 4));
+    uint4 vd = lds128(vs + (t1 + 8) * 128 + ((r ^ t1) << 4));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+
+    const int valid = min(kPage, L - (pg0 + i) * kPage);  // >= 1
+    if (valid < kPage) {  // tail page: unused slots may hold anything (even NaN)
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      if (t0 >= valid) va = z;
+      if (t1 >= valid) vb = z;
+      if (t0 + 8 >= valid) vc = z;
+      if (t1 + 8 >= valid) vd = z;
+    }
+
+    // S = Q K^T: two n-tiles of 8 tokens
+    float sc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      const uint4 ka = nt ? k1a : k0a, kb = nt ? k1b : k0b;
+      mma_16816_bf16(sc[nt], qa[0], ka.x, ka.y);
+      mma_16816_bf16(sc[nt], qa[1], ka.z, ka.w);
+      mma_16816_bf16(sc[nt], qa[2], kb.x, kb.y);
+      mma_16816_bf16(sc[nt], qa[3], kb.z, kb.w);
+    }
+    // scale to log2 units, mask slots past the sequence end
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = nt * 8 + 2 * qd + (e & 1);
+        sc[nt][e] = tok < valid ? sc[nt][e] * sl2 : -INFINITY;
+      }
+    }
+    float mx_r = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+    float mx_r8 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+    mx_r = fmaxf(mx_r, __shfl_xor_sync(0xffffffffu, mx_r, 1));
+    mx_r = fmaxf(mx_r, __shfl_xor_sync(0xffffffffu, mx_r, 2));
+    mx_r8 = fmaxf(mx_r8, __shfl_xor_sync(0xffffffffu, mx_r8, 1));
+    mx_r8 = fmaxf(mx_r8, __shfl_xor_sync(0xffffffffu, mx_r8, 2));
+    const float mn_r = fmaxf(m_r, mx_r), mn_r8 = fmaxf(m_r8, mx_r8);  // finite: the page has a valid slot
+    const float al_r = fast_exp2(m_r - mn_r), al_r8 = fast_exp2(m_r8 - mn_r8);
+    m_r = mn_r;
+    m_r8 = mn_r8;
+    float pr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      pr[nt][0] = fast_exp2(sc[nt][0] - mn_r);
+      pr[nt][1] = fast_exp2(sc[nt][1] - mn_r);
+      pr[nt][2] = fast_exp2(sc[nt][2] - mn_r8);
+      pr[nt][3] = fast_exp2(sc[nt][3] - mn_r8);
+    }
+    d_r = d_r * al_r + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+    d_r8 = d_r8 * al_r8 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+    uint32_t pa[4];
+    pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+    pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+    pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+    pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    // O = alpha * O + P V over 8 n-tiles of output dims
+    const uint32_t vaw[4] = {va.x, va.y, va.z, va.w}, vbw[4] = {vb.x, vb.y, vb.z, vb.w};
+    const uint32_t vcw[4] = {vc.x, vc.y, vc.z, vc.w}, vdw[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      o[j][0] *= al_r;
+      o[j][1] *= al_r;
+      o[j][2] *= al_r8;
+      o[j][3] *= al_r8;
+      const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+      const uint32_t b0 = __byte_perm(vaw[j >> 1], vbw[j >> 1], sel);
+      const uint32_t b1 = __byte_perm(vcw[j >> 1], vdw[j >> 1], sel);
+      mma_16816_bf16(o[j], pa, b0, b1);
+    }
+  }
+
+  // ---------------------------------------------- merge the four warps' states
+  d_r += __shfl_xor_sync(0xffffffffu, d_r, 1);
+  d_r += __shfl_xor_sync(0xffffffffu, d_r, 2);
+  d_r8 += __shfl_xor_sync(0xffffffffu, d_r8, 1);
+  d_r8 += __shfl_xor_sync(0xffffffffu, d_r8, 2);
+  named_barrier(1, kConsumerWarps * 32);  // every consumer is done with the ring
+  float* scr = reinterpret_cast<float*>(smem) + warp * kScratchFloatsPerWarp;
+  float* sm = scr;
+  float* sd = scr + kRows;
+  float* so = scr + 2 * kRows;
+  if (qd == 0) {
+    sm[r] = m_r;
+    sd[r] = d_r;
+    sm[r + 8] = m_r8;
+    sd[r + 8] = d_r8;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    so[r * kD + 16 * qd + j] = o[j][0];
+    so[r * kD + 16 * qd + 8 + j] = o[j][1];
+    so[(r + 8) * kD + 16 * qd + j] = o[j][2];
+    so[(r + 8) * kD + 16 * qd + 8 + j] = o[j][3];
+  }
+  named_barrier(1, kConsumerWarps * 32);
+
+  const int tid = threadIdx.x;  // 0..127
+  const int row = tid >> 3, c8 = (tid & 7) * 8;
+  if (row >= G) return;
+  const float* base = reinterpret_cast<const float*>(smem);
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, base[w * kScratchFloatsPerWarp + row]);
+  float W = 0.f, acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float* ws = base + w * kScratchFloatsPerWarp;
+      const float mw = ws[row];
+      if (mw == -INFINITY) continue;
+      const float f = fast_exp2(mw - M);
+      W += ws[kRows + row] * f;
+      const float* ow = ws + 2 * kRows + row * kD + c8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += ow[e] * f;
+    }
+  }
+  const int h = g * G + row;
+  if (p.direct) {
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    const size_t o_off = ((size_t)b * p.hq + h) * kD + c8;
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o_off);
+      dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+      dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+    } else {
+      uint4 v;
+      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = v;
+    }
+    if (p.lse && c8 == 0) p.lse[(size_t)b * p.hq + h] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+  } else {
+    const size_t slot = ((size_t)b * p.hq + h) * p.max_splits + s;
+    float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kD + c8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (c8 == 0) {
+      p.ws_md[slot * 2] = M;
+      p.ws_md[slot * 2 + 1] = W;
+    }
+  }
+}
+
+// Combine the chunks' partial states: one warp per (sequence, query head).
+// Lane l owns output dims 2l, 2l+1.  Chunk c contributes with weight
+// 2^(m_c - M), M = max_c m_c; chunks that saw nothing have m_c = -inf.
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int b = wid / p.hq, h = wid % p.hq;
+  if (b >= p.batch) return;
+  const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
+  int n, pg0, pg1;
+  chunk_range(p, L, 0, n, pg0, pg1);
+  const size_t slot0 = ((size_t)b * p.hq + h) * p.max_splits;
+  const float* md = p.ws_md + slot0 * 2;
+  float M = -INFINITY;
+  for (int c = lane; c < n; c += 32) M = fmaxf(M, md[2 * c]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float W = 0.f, a0 = 0.f, a1 = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < n; ++c) {
+      const float mc = md[2 * c];
+      if (mc == -INFINITY) continue;
+      const float f = fast_exp2(mc - M);
+      W += md[2 * c + 1] * f;
+      const float2 oc = *reinterpret_cast<const float2*>(p.ws_o + (slot0 + c) * kD + 2 * lane);
+      a0 += oc.x * f;
+      a1 += oc.y * f;
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  const size_t o_off = ((size_t)b * p.hq + h) * kD + 2 * lane;
+  if (p.out_f32) {
+    *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.out) + o_off) = make_float2(a0 * inv, a1 * inv);
+  } else {
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = pack_bf16x2(a0 * inv, a1 * inv);
+  }
+  if (p.lse && lane == 0) p.lse[(size_t)b * p.hq + h] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+}
+
+size_t decode_smem_bytes() { return kRingBytes + 2 * kStages * 8 + 16 + 1024; }
+int decode_threads() { return kThreads; }
+
+}  // namespace sa
+
+namespace sa {
+
+cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                          cudaStream_t stream) {
+  dim3 grid(p.max_splits, p.hkv, p.batch);
+  decode_split_kernel<<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.direct) return e;
+  const long long warps = (long long)p.batch * p.hq;
+  decode_merge_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -1,0 +1,55 @@
+// Internal interface of the split-KV decode kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sa {
+
+struct DecodeParams {
+  const __nv_bfloat16* q;     // [B, Hq, 64]
+  const int32_t* page_table;  // [B, stride]
+  const int32_t* seqlens;     // [B]
+  const float* sinks;         // [Hq]
+  void* out;                  // [B, Hq, 64] bf16 or fp32
+  float* lse;                 // [B, Hq] or null
+  float* ws_o;                // [B, Hq, max_splits, 64] partial weighted sums
+  float* ws_md;               // [B, Hq, max_splits, 2] partial (m, d), m in log2 units
+  unsigned* err;              // device error word
+  int batch, hq, hkv, group, stride;
+  int num_splits;   // > 0: requested chunks per sequence; 0: by length
+  int split_pages;  // pages per chunk when num_splits == 0
+  int max_splits;   // grid extent of the chunk dimension
+  int direct;       // 1: one chunk per sequence, write the output directly
+  int out_f32;
+  float scale_log2;  // scale * log2(e)
+  uint64_t wait_limit_ns;
+};
+
+// Number of chunks sequence with `npages` pages is cut into.  Every chunk is
+// non-empty (a sequence with no page still gets one chunk: the sink alone).
+__host__ __device__ inline int decode_num_chunks(int npages, int num_splits, int split_pages, int max_splits) {
+  if (npages <= 0) return 1;
+  int n = num_splits > 0 ? num_splits : (npages + split_pages - 1) / split_pages;
+  if (n > npages) n = npages;
+  if (n > max_splits) n = max_splits;
+  if (n < 1) n = 1;
+  const int chunk = (npages + n - 1) / n;
+  return (npages + chunk - 1) / chunk;
+}
+
+__global__ void decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                                    const DecodeParams p);
+__global__ void decode_merge_kernel(const DecodeParams p);
+
+size_t decode_smem_bytes();
+int decode_threads();
+
+// Enqueue the chunk kernel and, when chunks are merged, the merge kernel.
+cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                          cudaStream_t stream);
+
+}  // namespace sa

@@ -1,0 +1,459 @@
+// Causal variable-length prefill with a per-head sink logit (sm_103a).
+//
+// Method: Perplexity, "GPT-OSS on day 0", section "Sink Attention": the
+// softmax of every query row is taken over its (causal) key logits plus the
+// head's sink logit, evaluated online over key tiles with a running maximum m
+// and running scale d; the state starts at m = sink, d = 1, which counts the
+// sink once in the normaliser.  The sink has no value vector.
+//
+// Design (persistent, warp-specialised, one CTA per SM):
+//   * work unit = (sequence, 128-row query block, pair of query heads of one
+//     GQA group).  The two heads share every K/V tile, so a tile is staged once
+//     for two 128x128 score tiles.  Units are ordered longest first (query
+//     blocks with the most key tiles first), the heads of one group adjacent so
+//     that concurrently running CTAs read the same K/V from L2, and dealt to
+//     CTAs in a serpentine order.
+//   * warp 0 (one thread): TMA producer.  Loads the two 128x64 Q tiles of a
+//     unit, then K_0, V_0, K_1, V_1, ... through an 8-slot ring of 16 KiB
+//     tiles (128-byte swizzle), each slot guarded by a full/empty mbarrier.
+//   * warp 1 (one thread): MMA issuer.  S_t = Q_t K_j^T (M=128, N=128, K=64)
+//     into TMEM, and O_t += P_t V_j (M=128, N=64, K=128) with P_t read from
+//     TMEM (A operand) and V_j from shared memory (MN-major B operand).  Issue
+//     order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1) lets the tensor cores work
+//     on one head while the other head's softmax runs.
+//   * warps 4..7 / 8..11: softmax of head 0 / head 1, one thread per query row.
+//     Each reads its 128 scores from TMEM, applies the causal mask on the
+//     diagonal tile, updates (m, d), writes P (bf16) back over its scores, and
+//     at the end normalises O by d and stores the row.
+//   * warp 2 allocates / frees the 512 TMEM columns:
+//       S_0 [0,128)  S_1 [128,256)  O_0 [256,320)  O_1 [320,384)
+//     P_t occupies the first 64 columns of S_t (two bf16 per column).
+// The running maximum is only raised when a tile's maximum exceeds it by more
+// than 8 (log2 units), so O is rescaled rarely; the final O / d is exact for
+// any reference point, and P stays <= 2^8 which bf16 and fp32 hold easily.
+#include "common.cuh"
+#include "prefill.h"
+#include "tcgen05.cuh"
+
+#include <algorithm>
+
+namespace sa {
+
+namespace {
+
+constexpr int kTile = kPrefillTileRows;
+constexpr int kD = 64;
+constexpr int kTileBytes = kTile * kD * 2;  // 16 KiB
+constexpr int kSlots = 8;
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }   // S_t / P_t
+__host__ __device__ constexpr uint32_t col_o(int t) { return t ? 320u : 256u; }  // O_t
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
+constexpr float kRescaleThreshold = 8.f;
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 0;                                // 2 Q tiles
+constexpr int kOffRing = kOffQ + 2 * kTileBytes;         // kSlots K/V tiles
+constexpr int kOffBar = kOffRing + kSlots * kTileBytes;  // mbarriers
+constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 1;
+constexpr int kOffMisc = kOffBar + 256;
+constexpr int kOffSeq = kOffMisc + 64;
+constexpr int kSmemBytes = kOffSeq + 4 * kPrefillMaxBatch * 4 + 1024;
+static_assert(kNumBars * 8 <= 256, "barrier area");
+
+struct Bars {
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* slot_full;
+  uint64_t* slot_empty;
+  uint64_t* s_full;  // [2] MMA -> softmax: scores ready (and, last, O ready)
+  uint64_t* p_full;  // [2] softmax -> MMA: P written (and O rescaled)
+  uint64_t* drain;
+};
+
+// Walks the longest-first list of query blocks.  Level n holds the query
+// block n-1 of every sequence with at least n blocks; sequences are sorted by
+// block count, so level n's sequences are the first cnt(n) of the sorted list.
+struct Cursor {
+  const int* nqb;  // sorted, descending
+  int batch;
+  int level, cnt, start;
+  __device__ void init(const int* nqb_sorted, int b) {
+    nqb = nqb_sorted;
+    batch = b;
+    level = b > 0 ? nqb[0] : 0;
+    cnt = 0;
+    while (cnt < batch && nqb[cnt] >= level) ++cnt;
+    start = 0;
+  }
+  // qbl must not decrease between calls.  Returns the sorted sequence index.
+  __device__ int seek(int qbl, int& qb) {
+    while (qbl >= start + cnt) {
+      start += cnt;
+      --level;
+      while (cnt < batch && nqb[cnt] >= level) ++cnt;
+    }
+    qb = level - 1;
+    return qbl - start;
+  }
+};
+
+struct Unit {
+  int seq;  // sorted index
+  int qb;   // query block within the sequence
+  int g;    // kv head
+  int pair; // pair of query heads within the group
+};
+
+__device__ __forceinline__ bool next_unit(int k, int total, int pairs_per_group, int hkv, Cursor& cur, Unit& u) {
+  const int c = blockIdx.x, G = gridDim.x;
+  const long long idx = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
+  if (idx >= total) return false;
+  const int ui = (int)idx;
+  u.pair = ui % pairs_per_group;
+  const int rest = ui / pairs_per_group;
+  u.g = rest % hkv;
+  u.seq = cur.seek(rest / hkv, u.qb);
+  return true;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const PrefillParams& p,
+                                              volatile int* abort_flag) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, parity, p.err, kErrPrefill, p.wait_limit_ns)) return true;
+  *abort_flag = 1;
+  return false;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  Bars bars;
+  bars.q_full = bar_base;
+  bars.q_empty = bar_base + 1;
+  bars.slot_full = bar_base + 2;
+  bars.slot_empty = bars.slot_full + kSlots;
+  bars.s_full = bars.slot_empty + kSlots;
+  bars.p_full = bars.s_full + 2;
+  bars.drain = bars.p_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* total_qblocks = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  int* seq_start = reinterpret_cast<int*>(smem + kOffSeq);   // sorted
+  int* seq_len = seq_start + kPrefillMaxBatch;                // sorted
+  int* seq_nqb = seq_len + kPrefillMaxBatch;                  // sorted, descending
+  int* tmp_nqb = seq_nqb + kPrefillMaxBatch;                  // by batch index
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = p.batch;
+
+  // ---- per-CTA schedule table: sequences sorted by query-block count
+  for (int i = tid; i < B; i += kThreads) {
+    const int len = max(0, __ldg(p.cu_seqlens + i + 1) - __ldg(p.cu_seqlens + i));
+    tmp_nqb[i] = (len + kTile - 1) / kTile;
+  }
+  if (tid == 0) {
+    mbar_init(bars.q_full, 1);
+    mbar_init(bars.q_empty, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bars.slot_full + i, 1);
+      mbar_init(bars.slot_empty + i, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.s_full + t, 1);
+      mbar_init(bars.p_full + t, 128);  // every softmax thread of the head arrives
+    }
+    mbar_init(bars.drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  for (int i = tid; i < B; i += kThreads) {
+    const int mine = tmp_nqb[i];
+    int rank = 0, total = 0;
+    for (int j = 0; j < B; ++j) {
+      const int o = tmp_nqb[j];
+      rank += (o > mine) || (o == mine && j < i);
+      total += o;
+    }
+    const int st = __ldg(p.cu_seqlens + i);
+    seq_start[rank] = st;
+    seq_len[rank] = max(0, __ldg(p.cu_seqlens + i + 1) - st);
+    seq_nqb[rank] = mine;
+    if (i == 0) *total_qblocks = total;
+  }
+  tc_fence_after();
+  __syncthreads();
+  const uint32_t tmem = *tmem_holder;
+  const int pairs_per_group = (p.group + 1) / 2;
+  const long long total_ll = (long long)(*total_qblocks) * p.hkv * pairs_per_group;
+  const int total_units = (int)min(total_ll, (long long)0x7fffffff);
+  Cursor cur;
+  cur.init(seq_nqb, B);
+
+  uint8_t* q_tile[2] = {smem + kOffQ, smem + kOffQ + kTileBytes};
+  uint8_t* ring = smem + kOffRing;
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      const uint64_t pol_stream = l2_policy_evict_first();
+      uint32_t ring_i = 0;
+      Unit u;
+      for (int k = 0; next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+        if (k > 0 && !wait_or_abort(bars.q_empty, (k - 1) & 1, p, abort_flag)) break;
+        const int t0 = seq_start[u.seq] + u.qb * kTile;
+        const int hA = u.g * p.group + 2 * u.pair;
+        const int hB = (2 * u.pair + 1 < p.group) ? hA + 1 : hA;
+        mbar_arrive_expect_tx(bars.q_full, 2 * kTileBytes);
+        tma_load_3d_hint(q_tile[0], &qmap, bars.q_full, 0, hA, t0, pol_stream);
+        tma_load_3d_hint(q_tile[1], &qmap, bars.q_full, 0, hB, t0, pol_stream);
+        const int kv0 = seq_start[u.seq];
+        const int n = u.qb + 1;
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int slot = ring_i % kSlots;
+            if (ring_i >= kSlots && !wait_or_abort(bars.slot_empty + slot, ((ring_i / kSlots) - 1) & 1, p, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bars.slot_full + slot, kTileBytes);
+            tma_load_3d(ring + slot * kTileBytes, kv ? &vmap : &kmap, bars.slot_full + slot, 0, u.g,
+                        kv0 + j * kTile);
+            ++ring_i;
+          }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA can exit
+        for (uint32_t i = ring_i > kSlots ? ring_i - kSlots : 0; i < ring_i; ++i)
+          mbar_wait(bars.slot_full + (i % kSlots), (i / kSlots) & 1, p.err, kErrPrefill, 10000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      uint32_t ring_i = 0, pph[2] = {0, 0};
+      const uint64_t dq[2] = {smem_desc_sw128(smem_addr(q_tile[0])), smem_desc_sw128(smem_addr(q_tile[1]))};
+      Unit u;
+      bool ok = true;
+      for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+        const int n = u.qb + 1;
+        if (!(ok = wait_or_abort(bars.q_full, k & 1, p, abort_flag))) break;
+        // K_0 -> S_0, S_1
+        uint32_t kslot = ring_i % kSlots;
+        if (!(ok = wait_or_abort(bars.slot_full + kslot, (ring_i / kSlots) & 1, p, abort_flag))) break;
+        tc_fence_after();
+        uint64_t dk = smem_desc_sw128(smem_addr(ring + kslot * kTileBytes));
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) umma_ss(tmem + col_s(t), dq[t] + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);
+          umma_commit(bars.s_full + t);
+        }
+        umma_commit(bars.slot_empty + kslot);
+        if (n == 1) umma_commit(bars.q_empty);
+        ++ring_i;
+        for (int j = 0; j < n; ++j) {
+          const uint32_t vslot = ring_i % kSlots;
+          if (!(ok = wait_or_abort(bars.slot_full + vslot, (ring_i / kSlots) & 1, p, abort_flag))) break;
+          const uint64_t dv = smem_desc_sw128(smem_addr(ring + vslot * kTileBytes));
+          const bool more = j + 1 < n;
+          if (more) {
+            kslot = (ring_i + 1) % kSlots;
+            if (!(ok = wait_or_abort(bars.slot_full + kslot, ((ring_i + 1) / kSlots) & 1, p, abort_flag))) break;
+            dk = smem_desc_sw128(smem_addr(ring + kslot * kTileBytes));
+          }
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!(ok = wait_or_abort(bars.p_full + t, pph[t], p, abort_flag))) break;
+            pph[t] ^= 1;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + 128 * kk, kIdescPV, (j > 0) || (kk > 0));
+            if (t == 1) umma_commit(bars.slot_empty + vslot);
+            if (more) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) umma_ss(tmem + col_s(t), dq[t] + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);
+            }
+            umma_commit(bars.s_full + t);  // scores of tile j+1, or the finished O
+          }
+          if (!ok) break;
+          if (more) {
+            umma_commit(bars.slot_empty + kslot);
+            if (j + 2 == n) umma_commit(bars.q_empty);
+            ring_i += 2;
+          } else {
+            ring_i += 1;
+          }
+        }
+      }
+      // every MMA issued by this thread must finish before TMEM is released
+      umma_commit(bars.drain);
+      mbar_wait(bars.drain, 0, p.err, kErrPrefill, p.wait_limit_ns);
+    }
+  } else if (warp >= 4) {
+    // ================================================================ softmax
+    const int t = (warp - 4) >> 2;         // which query tile (head of the pair)
+    const int quad = warp & 3;             // TMEM lane quarter of this warp
+    const int r = quad * 32 + lane;        // query row within the tile
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + col_s(t);
+    const uint32_t o_addr = tmem + lane_off + col_o(t);
+    const float sl2 = p.scale_log2;
+    uint32_t sph = 0;
+    Unit u;
+    bool ok = true;
+    for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+      const int n = u.qb + 1;
+      const int h = u.g * p.group + 2 * u.pair + t;
+      const bool head_ok = 2 * u.pair + t < p.group;
+      float m = head_ok ? __ldg(p.sinks + h) * kLog2e : -INFINITY;  // sink-seeded state
+      float d = 1.f;
+      for (int j = 0; j < n; ++j) {
+        ok = wait_or_abort(bars.s_full + t, sph, p, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        sph ^= 1;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+        tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_ld_wait();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        if (j == n - 1) {  // diagonal tile: key c is visible to row r iff c <= r
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > r) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const bool need = m_tile > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? m_tile : m;
+          const float alpha = fast_exp2(m - m_new);
+          d *= alpha;
+          if (j > 0) {  // O holds tiles 0..j-1 (their MMAs completed before S_j was signalled)
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+              uint32_t ob[16];
+              tmem_ld16(o_addr + c0, ob);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) ob[e] = __float_as_uint(__uint_as_float(ob[e]) * alpha);
+              tmem_st16(o_addr + c0, ob);
+            }
+          }
+          m = m_new;
+        }
+        const float neg_m = -m;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = fast_exp2(fmaf(s[half * 64 + 2 * i], sl2, neg_m));
+            const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * i + 1], sl2, neg_m));
+            sum0 += p0;
+            sum1 += p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(s_addr + half * 32, pk);
+        }
+        tmem_st_wait();
+        d += sum0 + sum1;
+        tc_fence_before();
+        mbar_arrive(bars.p_full + t);
+      }
+      if (!ok) break;
+      // ---- epilogue: wait for the last PV, normalise, store
+      ok = wait_or_abort(bars.s_full + t, sph, p, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      sph ^= 1;
+      tc_fence_after();
+      uint32_t ob[64];
+      tmem_ld32(o_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&ob[0]));
+      tmem_ld32(o_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&ob[32]));
+      tmem_ld_wait();
+      const int row_tok = u.qb * kTile + r;
+      const int tok = seq_start[u.seq] + row_tok;  // checked against T too: cu_seqlens is not trusted
+      if (head_ok && row_tok < seq_len[u.seq] && tok >= 0 && tok < p.total_tokens) {
+        const float inv = 1.f / d;
+        const size_t row = (size_t)tok * p.hq + h;
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * kD);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            dst[i] = make_float4(__uint_as_float(ob[4 * i]) * inv, __uint_as_float(ob[4 * i + 1]) * inv,
+                                 __uint_as_float(ob[4 * i + 2]) * inv, __uint_as_float(ob[4 * i + 3]) * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * kD);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ob[8 * i + 0]) * inv, __uint_as_float(ob[8 * i + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(ob[8 * i + 2]) * inv, __uint_as_float(ob[8 * i + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(ob[8 * i + 4]) * inv, __uint_as_float(ob[8 * i + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(ob[8 * i + 6]) * inv, __uint_as_float(ob[8 * i + 7]) * inv);
+            dst[i] = v;
+          }
+        }
+        if (p.lse) p.lse[row] = (m + __log2f(d)) * kLn2;
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+cudaError_t prefill_configure() {
+  return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const PrefillParams& p, int num_sms, cudaStream_t stream) {
+  const long long ppg = (p.group + 1) / 2;
+  const long long upper = ppg * p.hkv * ((long long)(p.total_tokens + kTile - 1) / kTile + p.batch);
+  const int grid = (int)std::min<long long>(std::max(1, num_sms), std::max(1LL, upper));
+  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -1,0 +1,166 @@
+/*
+ * sink_attn.h -- C ABI of the GB300 (sm_103a) sink-attention library.
+ *
+ * Grouped-query attention in which every query head owns one trained "sink"
+ * logit that joins the softmax normaliser but carries no value vector
+ * (Perplexity, "GPT-OSS on day 0": model overview, attention bullet, and the
+ * section "Sink Attention").  For query head h, kv head g = h / (Hq / Hkv),
+ * and the keys j visible to a query:
+ *
+ *     s_j    = scale * <q_h, k_{j,g}>
+ *     M      = max(max_j s_j, sink_h)
+ *     Z      = sum_j exp(s_j - M) + exp(sink_h - M)
+ *     out_h  = sum_j exp(s_j - M) / Z * v_{j,g}
+ *     lse_h  = M + log(Z)              (natural log, includes the sink)
+ *
+ * The kernels evaluate this with an online softmax whose running maximum
+ * starts at the head's sink and whose running scale starts at 1 (same
+ * section, closing paragraph); when the key length is split into chunks,
+ * only the first chunk is seeded with the sink.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no reference to them after the call returns.
+ *   - bf16 means IEEE bfloat16 stored in 2 bytes; tensors are dense and
+ *     row-major in the order of the dimensions listed (no strides).
+ *   - Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously on it; the call returns before it finishes.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     non-zero status means nothing was enqueued and no output was written
+ *     (SINK_ATTN_ERR_CUDA can also report a failed launch).
+ *   - No C++ exception crosses this interface.
+ *   - Supported: head_dim == 64, page_size == 16, scale > 0 and finite,
+ *     Hq % Hkv == 0.  Sinks may be -inf (no sink).  +inf / NaN sinks are
+ *     outside the contract.
+ *   - Device-side waits are bounded; a wait that gives up records a timeout
+ *     that sink_attn_get_device_error() reports.
+ */
+#ifndef SINK_ATTN_H_
+#define SINK_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SINK_ATTN_OK = 0,
+  SINK_ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or count */
+  SINK_ATTN_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement */
+  SINK_ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  SINK_ATTN_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
+  SINK_ATTN_ERR_NO_MEMORY = 5    /* workspace allocation failed */
+} sink_attn_status;
+
+typedef enum {
+  SINK_ATTN_OUT_BF16 = 0, /* out is bf16 */
+  SINK_ATTN_OUT_F32 = 1   /* out is fp32 */
+} sink_attn_out_dtype;
+
+/*
+ * Causal variable-length prefill ("GPT-OSS on day 0", section Sink Attention,
+ * applied to every query of a packed batch; query length = key length).
+ *
+ *   q           bf16 [total_tokens, num_q_heads, head_dim]
+ *   k, v        bf16 [total_tokens, num_kv_heads, head_dim]
+ *   sinks       fp32 [num_q_heads] (per query head, not multiplied by scale)
+ *   cu_seqlens  int32 [batch + 1], DEVICE memory: cu[0] = 0, non-decreasing,
+ *               cu[batch] = total_tokens.  Sequence b owns tokens
+ *               [cu[b], cu[b+1]); token i of a sequence sees keys 0..i of the
+ *               same sequence.  Zero-length sequences are allowed.
+ *   batch, total_tokens, max_seqlen
+ *               host copies used to size the grid without a device sync;
+ *               max_seqlen must be >= every sequence length.
+ *   scale       softmax scale applied to q.k (typically 1/sqrt(head_dim)).
+ *               k and v must be finite everywhere: key tiles are 128 tokens
+ *               long, and the tail of a sequence's last tile (tokens of the next
+ *               sequence) enters the value product with weight exactly 0.
+ *   out         [total_tokens, num_q_heads, head_dim], bf16 or fp32 per
+ *               out_dtype.  Written for every token of every sequence.
+ *   lse         optional fp32 [total_tokens, num_q_heads] (natural-log
+ *               normaliser including the sink); NULL to skip.
+ * Limits: batch <= 1024; max_seqlen < 2^24; total_tokens * num_q_heads < 2^31.
+ * batch == 0 or total_tokens == 0 is a no-op returning SINK_ATTN_OK.
+ */
+int sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                      const int32_t* cu_seqlens, int batch, int total_tokens, int max_seqlen,
+                      int num_q_heads, int num_kv_heads, int head_dim, float scale,
+                      void* out, int out_dtype, float* lse, void* stream);
+
+/*
+ * Split-KV decode: one query token per sequence against a paged KV cache
+ * ("GPT-OSS on day 0", section Sink Attention: the key length is split into
+ * chunks and only the first chunk's online state starts from the sink).
+ *
+ *   q           bf16 [batch, num_q_heads, head_dim]
+ *   k_pages,    bf16 [num_pages, num_kv_heads, page_size, head_dim]: one
+ *   v_pages     (page, kv head) slab is page_size*head_dim contiguous values.
+ *   page_table  int32 [batch, page_table_stride], DEVICE: token j of
+ *               sequence b lives in page page_table[b][j / page_size], slot
+ *               j % page_size.  Only the first ceil(seqlens[b]/page_size)
+ *               entries of a row are read; each must be in [0, num_pages).
+ *   seqlens     int32 [batch], DEVICE: number of cached tokens of each
+ *               sequence (the query sees all of them).  A length of 0 gives
+ *               out = 0 (only the sink is in the softmax).
+ *   batch, max_seqlen, num_pages
+ *               host values: max_seqlen >= every seqlens[b] and
+ *               max_seqlen <= page_table_stride * page_size.
+ *   sinks       fp32 [num_q_heads]
+ *   num_q_heads / num_kv_heads must be <= 16 (one MMA row block per group).
+ *   num_splits  > 0: every sequence is split into that many chunks of pages
+ *               (fewer if it has fewer pages); 0: chosen per sequence length
+ *               by the library.  At most 256.
+ *   out         [batch, num_q_heads, head_dim], bf16 or fp32 per out_dtype.
+ *   lse         optional fp32 [batch, num_q_heads]; NULL to skip.
+ *   workspace   device scratch for the per-chunk partial states, at least
+ *               sink_attn_decode_workspace_bytes(...) bytes, 256-byte
+ *               aligned.  NULL: the library allocates and frees it in stream
+ *               order (cudaMallocAsync / cudaFreeAsync) when it is needed.
+ * batch == 0 is a no-op returning SINK_ATTN_OK.
+ */
+int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages,
+                     const int32_t* page_table, int page_table_stride,
+                     const int32_t* seqlens, int batch, int max_seqlen, int num_pages,
+                     const float* sinks, int num_q_heads, int num_kv_heads, int head_dim,
+                     int page_size, float scale, int num_splits,
+                     void* out, int out_dtype, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace sink_attn_decode needs for these arguments (0 when no
+ * sequence is split, i.e. the chunks write the output directly).  Returns
+ * (size_t)-1 for arguments sink_attn_decode would reject.
+ */
+size_t sink_attn_decode_workspace_bytes(int batch, int max_seqlen, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int page_size,
+                                        int num_splits);
+
+/*
+ * The largest number of chunks any sequence gets for these arguments
+ * (the grid's chunk dimension); 0 for arguments sink_attn_decode would reject.
+ */
+int sink_attn_decode_max_splits(int batch, int max_seqlen, int num_kv_heads, int page_size,
+                                int num_splits);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* sink_attn_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reports (and clears) any timeout recorded by a
+ * bounded device-side wait on the current device since the last call:
+ * SINK_ATTN_OK, SINK_ATTN_ERR_TIMEOUT, or SINK_ATTN_ERR_CUDA if the sync or
+ * the read failed.
+ */
+int sink_attn_get_device_error(void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int sink_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINK_ATTN_H_ */

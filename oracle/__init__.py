@@ -10,5 +10,6 @@ from .sink_attention import (  # noqa: F401
     gather_paged_kv,
     online_split_merge,
     prefill,
+    prefill_rows,
     sink_softmax_rows,
 )

@@ -51,6 +51,7 @@ __all__ = [
     "sink_softmax_rows",
     "attend_rows",
     "prefill",
+    "prefill_rows",
     "decode",
     "gather_paged_kv",
     "online_split_merge",
@@ -169,19 +170,53 @@ def prefill(q, k, v, sinks, cu_seqlens, scale: float):
     return out, lse
 
 
+def prefill_rows(q, k, v, sinks, cu_seqlens, scale: float, tokens, heads):
+    """The prefill definition evaluated only at selected (token, head) pairs.
+
+    Same arithmetic as ``prefill`` (row i of a sequence sees keys 0..i of that
+    sequence), for the cross product of ``tokens`` (packed token indices) and
+    ``heads``; only the keys each row needs are upcast.  Inputs may be CPU
+    torch tensors or numpy arrays.  Returns (out [len(tokens), len(heads), D],
+    lse [len(tokens), len(heads)]).
+    """
+    cu = _as_int(cu_seqlens)
+    sinks = _as_f64(sinks)
+    hq = q.shape[1]
+    hkv = k.shape[1]
+    group = hq // hkv
+    tokens = [int(t) for t in tokens]
+    heads = [int(h) for h in heads]
+    d = q.shape[2]
+    out = np.zeros((len(tokens), len(heads), d))
+    lse = np.zeros((len(tokens), len(heads)))
+    for ti, t in enumerate(tokens):
+        b = int(np.searchsorted(cu, t, side="right")) - 1
+        t0 = int(cu[b])
+        keys = slice(t0, t + 1)  # causal: keys of the same sequence up to t
+        for hi, h in enumerate(heads):
+            g = h // group
+            kk = _as_f64(k[keys, g, :])
+            vv = _as_f64(v[keys, g, :])
+            s = scale * (_as_f64(q[t, h, :])[None, :] @ kk.T)
+            o, l = attend_rows(s, float(sinks[h]), vv)
+            out[ti, hi] = o[0]
+            lse[ti, hi] = l[0]
+    return out, lse
+
+
 def gather_paged_kv(pages, page_table_row, length: int, page_size: int):
     """Contiguous [length, Hkv, D] view of one sequence's paged cache.
 
     pages : [num_pages, Hkv, page_size, D]; token j of the sequence lives at
-    pages[page_table_row[j // page_size], :, j % page_size, :].
+    pages[page_table_row[j // page_size], :, j % page_size, :].  Only the
+    pages the sequence owns are read (and upcast).
     """
-    pages = _as_f64(pages)
     row = _as_int(page_table_row)
     n_pages = (length + page_size - 1) // page_size
     hkv, d = pages.shape[1], pages.shape[3]
     out = np.zeros((n_pages * page_size, hkv, d))
     for p in range(n_pages):
-        out[p * page_size:(p + 1) * page_size] = pages[int(row[p])].transpose(1, 0, 2)
+        out[p * page_size:(p + 1) * page_size] = _as_f64(pages[int(row[p])]).transpose(1, 0, 2)
     return out[:length]
 
 
@@ -198,8 +233,7 @@ def decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: float,
     table = _as_int(page_table)
     lens = _as_int(seqlens)
     B, hq, d = q.shape
-    kp = _as_f64(k_pages)
-    vp = _as_f64(v_pages)
+    kp, vp = k_pages, v_pages  # gathered (and upcast) per sequence below
     hkv = kp.shape[1]
     group = hq // hkv
     out = np.zeros((B, hq, d))

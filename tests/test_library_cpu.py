@@ -1,0 +1,141 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+The library must build, load on a machine without a GPU, export every entry
+point include/sink_attn.h declares, and reject bad arguments on the host
+before touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gqa_attention_head_sink_gb300 as sa
+from gqa_attention_head_sink_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sink_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return sa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sink_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ["sink_attn_prefill", "sink_attn_decode", "sink_attn_decode_workspace_bytes",
+                 "sink_attn_status_string", "sink_attn_get_device_error"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in sink_attn.h but not exported"
+        assert name in binding.EXPORTS, f"{name} has no Python binding"
+
+
+def test_library_has_no_gpu_runtime_dependency():
+    # static CUDA runtime, driver reached at run time: loads on CPU-only hosts
+    out = os.popen(f"readelf -d {build.LIB}").read()
+    needed = re.findall(r"Shared library: \[(.*?)\]", out)
+    assert not any(n.startswith("libcudart") or n.startswith("libcuda.") for n in needed), needed
+
+
+def test_status_strings(lib):
+    assert sa.sink_attn_status_string(0) == "ok"
+    assert sa.sink_attn_status_string(4) == "device-side wait timed out"
+    assert sa.sink_attn_status_string(99) == "unknown status"
+    assert sa.sink_attn_version() >= 100
+
+
+def _decode_call(lib, **kw):
+    args = dict(q=8 * 16, k=8 * 32, v=8 * 48, table=8 * 64, stride=4, seqlens=8 * 80, batch=2, max_seqlen=64,
+                num_pages=8, sinks=8 * 96, hq=8, hkv=2, d=64, page=16, scale=0.125, splits=0, out=8 * 112,
+                out_dtype=1, lse=None, ws=None, ws_bytes=0)
+    args.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731  (fake, never dereferenced)
+    return lib.sink_attn_decode(P(args["q"]), P(args["k"]), P(args["v"]), P(args["table"]), args["stride"],
+                                P(args["seqlens"]), args["batch"], args["max_seqlen"], args["num_pages"],
+                                P(args["sinks"]), args["hq"], args["hkv"], args["d"], args["page"],
+                                args["scale"], args["splits"], P(args["out"]), args["out_dtype"], P(args["lse"]),
+                                P(args["ws"]), args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=128), 2),                 # head_dim 64 only
+    (dict(page=32), 2),               # page size 16 only
+    (dict(hq=7), 1),                  # Hq % Hkv != 0
+    (dict(hq=64, hkv=2), 2),          # group of 32 query heads: more than one MMA row block
+    (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(splits=-1), 1),
+    (dict(splits=257), 1),
+    (dict(out_dtype=7), 1),
+    (dict(q=None), 1),
+    (dict(q=8 * 16 + 4), 1),          # misaligned
+    (dict(stride=3), 1),              # page table too narrow for max_seqlen
+    (dict(num_pages=0), 1),
+    (dict(batch=-1), 1),
+    (dict(ws=8 * 128 + 64, ws_bytes=1 << 20), 1),  # workspace not 256-byte aligned
+    (dict(ws=256 * 4096, ws_bytes=16, splits=2), 1),  # workspace too small
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _decode_call(lib, **kw) == status
+
+
+def test_decode_empty_batch_is_noop(lib):
+    assert _decode_call(lib, batch=0, q=None, out=None) == 0
+
+
+def _prefill_call(lib, **kw):
+    args = dict(q=8 * 16, k=8 * 32, v=8 * 48, sinks=8 * 64, cu=8 * 80, batch=2, total=300, max_seqlen=200,
+                hq=8, hkv=2, d=64, scale=0.125, out=8 * 96, out_dtype=1, lse=None)
+    args.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.sink_attn_prefill(P(args["q"]), P(args["k"]), P(args["v"]), P(args["sinks"]), P(args["cu"]),
+                                 args["batch"], args["total"], args["max_seqlen"], args["hq"], args["hkv"],
+                                 args["d"], args["scale"], P(args["out"]), args["out_dtype"], P(args["lse"]), None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), 2),
+    (dict(hq=6, hkv=4), 1),
+    (dict(scale=-1.0), 1),
+    (dict(max_seqlen=301), 1),        # longer than the packed batch
+    (dict(batch=5000), 2),            # schedule table holds 1024 sequences
+    (dict(cu=None), 1),
+    (dict(out=8 * 96 + 2), 1),
+    (dict(out_dtype=3), 1),
+])
+def test_prefill_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _prefill_call(lib, **kw) == status
+
+
+def test_prefill_empty_is_noop(lib):
+    assert _prefill_call(lib, batch=0) == 0
+    assert _prefill_call(lib, total=0, max_seqlen=0) == 0
+
+
+def test_decode_planning(lib):
+    # fixed splits: at most one chunk per page
+    assert sa.sink_attn_decode_max_splits(64, 8192, 8, 16, 8) == 8
+    assert sa.sink_attn_decode_max_splits(4, 20, 8, 16, 8) == 2
+    # chosen per length: enough chunks to fill the GPU, 16..128 pages each
+    assert sa.sink_attn_decode_max_splits(128, 32768, 8, 16, 0) == 16
+    assert sa.sink_attn_decode_max_splits(1, 8192, 8, 16, 0) == 32
+    assert sa.sink_attn_decode_max_splits(1, 16, 8, 16, 0) == 1
+    # a single chunk writes the output directly: no workspace
+    assert sa.sink_attn_decode_workspace_bytes(4, 16, 64, 8, 64, 16, 0) == 0
+    n = sa.sink_attn_decode_workspace_bytes(64, 8192, 64, 8, 64, 16, 8)
+    slots = 64 * 64 * 8
+    assert n == slots * 64 * 4 + slots * 2 * 4
+    with pytest.raises(sa.SinkAttnError):
+        sa.sink_attn_decode_workspace_bytes(1, 16, 64, 8, 128, 16, 0)

@@ -304,3 +304,14 @@ def test_oracle_takes_bf16_values_exactly():
     out_n, _ = oracle.prefill(inp.q.float().numpy().astype(np.float64), inp.k.float().numpy(),
                               inp.v.float().numpy(), inp.sinks.numpy(), inp.cu_seqlens.numpy(), inp.scale)
     np.testing.assert_array_equal(out_t, out_n)
+
+
+def test_prefill_rows_agrees_with_full_definition():
+    inp = workloads.make_prefill([5, 130, 1, 64], num_q_heads=6, num_kv_heads=2, head_dim=16, seed=3,
+                                 sink_mode="mixed")
+    out, lse = oracle.prefill(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, inp.scale)
+    toks = [0, 4, 5, 6, 134, 135, 136, 199]
+    heads = [0, 3, 5]
+    o2, l2 = oracle.prefill_rows(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, inp.scale, toks, heads)
+    np.testing.assert_allclose(o2, out[toks][:, heads], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(l2, lse[toks][:, heads], rtol=0, atol=1e-14)

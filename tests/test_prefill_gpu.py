@@ -1,0 +1,133 @@
+"""GPU parity of causal varlen prefill against the float64 oracle.
+
+All calls go through the C ABI.  Small and medium cases (several 128-row
+tiles, ragged tails, empty and one-token sequences, odd GQA groups, every
+sink edge case) are compared on every element; the full-size workloads
+(one 8192-token sequence with 64/8 heads, and 16 ragged sequences of
+256..32768 tokens) are compared on sampled rows covering tile boundaries,
+sequence starts and ends, for every head.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gqa_attention_head_sink_gb300 as sa
+import oracle
+from gqa_attention_head_sink_gb300 import build, workloads
+from tests.parity import assert_parity, lse_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    build.build()
+    sa.load()
+    yield
+    assert sa.sink_attn_get_device_error() == 0, "a bounded device wait timed out"
+
+
+def run(inp, out_dtype=torch.float32, with_lse=False):
+    lse = torch.empty((inp.total_tokens, inp.num_q_heads), dtype=torch.float32, device="cuda") if with_lse else None
+    out = sa.sink_attn_prefill(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, inp.scale, out_dtype=out_dtype,
+                               lse=lse, max_seqlen=inp.max_seqlen)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def full_oracle(inp):
+    return oracle.prefill(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu(), inp.scale)
+
+
+def sampled_rows(seqlens, extra=()):
+    """Token indices at sequence starts/ends and 128-row tile boundaries."""
+    toks, start = set(extra), 0
+    for L in seqlens:
+        for r in (0, 1, 126, 127, 128, 129, L // 2, L - 129, L - 128, L - 2, L - 1):
+            if 0 <= r < L:
+                toks.add(start + r)
+        start += L
+    return sorted(toks)
+
+
+def test_prefill_tiny_workload():
+    inp = workloads.workload("tiny_prefill", device="cuda")
+    want, want_lse = full_oracle(inp)
+    out, lse = run(inp, with_lse=True)
+    assert_parity(out, want)
+    lse_close(lse, want_lse)
+    out_bf, _ = run(inp, out_dtype=torch.bfloat16)
+    assert_parity(out_bf, want, bf16_output=True)
+
+
+CASES = [
+    # lengths, Hq, Hkv, sink mode
+    ([1, 127, 128, 129, 300, 0, 517], 8, 2, "mixed"),
+    ([256, 255, 257], 16, 2, "normal2"),
+    ([200, 65], 6, 2, "normal1"),        # odd group: the second head of a pair is absent
+    ([333], 4, 4, "neginf"),              # plain MHA without sinks
+    ([1000, 1], 64, 8, "mixed"),
+    ([129] * 7, 4, 1, "zero"),
+]
+
+
+@pytest.mark.parametrize("lens,hq,hkv,sink", CASES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_prefill_small(lens, hq, hkv, sink, out_dtype):
+    inp = workloads.make_prefill(lens, num_q_heads=hq, num_kv_heads=hkv, seed=sum(lens) % 97, sink_mode=sink,
+                                 device="cuda")
+    want, want_lse = full_oracle(inp)
+    out, lse = run(inp, out_dtype=out_dtype, with_lse=True)
+    assert_parity(out, want, bf16_output=out_dtype == torch.bfloat16)
+    lse_close(lse, want_lse)
+
+
+def test_prefill_many_short_sequences():
+    g = torch.Generator().manual_seed(3)
+    lens = [int(x) for x in torch.randint(0, 300, (200,), generator=g)]
+    inp = workloads.make_prefill(lens, num_q_heads=16, num_kv_heads=2, seed=21, sink_mode="mixed", device="cuda")
+    want, _ = full_oracle(inp)
+    out, _ = run(inp)
+    assert_parity(out, want)
+
+
+def test_prefill_is_deterministic():
+    inp = workloads.make_prefill([700, 1300], seed=8, device="cuda")
+    a, _ = run(inp)
+    b, _ = run(inp)
+    assert torch.equal(a, b)
+
+
+def test_prefill_sequences_do_not_leak_into_each_other():
+    # changing one sequence's tokens must not change another sequence's output
+    inp = workloads.make_prefill([300, 260], num_q_heads=8, num_kv_heads=1, seed=9, device="cuda")
+    a, _ = run(inp)
+    inp.k[300:] = 100.0
+    inp.v[300:] = 1000.0
+    b, _ = run(inp)
+    assert torch.equal(a[:300], b[:300])
+
+
+@pytest.mark.slow
+def test_prefill_full_len8192():
+    inp = workloads.workload("gptoss_prefill", device="cuda")
+    out, lse = run(inp, with_lse=True)
+    toks = sampled_rows(inp.seqlens, extra=(1000, 4095, 4096, 6000))
+    heads = list(range(inp.num_q_heads))
+    cpu = (inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu())
+    want, want_lse = oracle.prefill_rows(*cpu, inp.scale, toks, heads)
+    assert_parity(out[toks], want)
+    lse_close(lse[toks], want_lse)
+
+
+@pytest.mark.slow
+def test_prefill_full_ragged16():
+    inp = workloads.workload("ragged_prefill", device="cuda")
+    out, _ = run(inp)
+    toks = sampled_rows(inp.seqlens)
+    rng = np.random.default_rng(0)
+    toks = sorted(rng.choice(toks, size=min(len(toks), 96), replace=False).tolist())
+    heads = list(range(inp.num_q_heads))
+    cpu = (inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu())
+    want, _ = oracle.prefill_rows(*cpu, inp.scale, toks, heads)
+    assert_parity(out[toks], want)
