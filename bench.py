@@ -1,0 +1,454 @@
+"""Benchmark of the sink-attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill: causal, one sequence of 8192 tokens, Hq=64, Hkv=8, D=64, bf16
+    q/k/v ~ N(0,1), sinks ~ N(0,2), scale 1/8 (the gpt-oss-shaped prefill);
+  * decode: 64 sequences x 8192 cached tokens, one query each, paged bf16 KV
+    (16-token pages, randomly permuted page table), 8 chunks per sequence,
+    merged.
+Inputs are resident in HBM before timing starts.  Between timed steps a
+256 MiB buffer is written to flush L2 (the prefill's 80 MiB of inputs would
+otherwise stay cached); the flush is outside the timed events.
+
+Reported (rank 0, one JSON line): `value` = prefill TFLOP/s (algorithmic
+flops: 4*D per unmasked query-key pair per query head) summed over ranks;
+`decode` = HBM GB/s of algorithmic bytes (K/V of every cached token once,
+queries, outputs, page-table entries); `roofline` for the prefill kernel
+(tensor bound) and decode (HBM bound) against the measured peaks of this
+GPU pool; `e2e` = the same through host buffers with the copies timed;
+`cpu_baseline` = the float64 oracle timed on a bounded sample on this host.
+
+`--impl reference` times the float64 CPU oracle (the only implementation the
+method's source provides a definition for) on bounded samples of the same
+workload and prints the same line with "impl": "reference".
+
+Several GPUs (torchrun): every rank runs its own replica of the workload
+(weak scaling, no collective on the data path); the timed region is
+bracketed by a barrier and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gqa_attention_head_sink_gb300 import workloads  # noqa: E402
+
+METRIC = "sink-attn prefill TFLOP/s and decode HBM GB/s, % of GB300 roofline"
+PREFILL = "gptoss_prefill"
+DECODE = "decode"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return None, 0, 1
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend)
+    return dist, dist.get_rank(), ws
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gqa_attention_head_sink_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+PREFILL_SOURCES = ["prefill.cu", "prefill.h", "tcgen05.cuh", "common.cuh"]
+DECODE_SOURCES = ["decode.cu", "decode.h", "common.cuh"]
+
+
+def _traffic(kernel: str, files):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
+    source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = _kernel_hash(files)
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel and parts[1] == want:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _events():
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def run_ours(args, dist, rank, world):
+    import gqa_attention_head_sink_gb300 as sa
+    from gqa_attention_head_sink_gb300 import build
+
+    if rank == 0 or dist is None:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    sa.load()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    pre = workloads.workload(PREFILL, device=dev)
+    dec = workloads.workload(DECODE, device=dev)
+    out_p = torch.empty(pre.q.shape, dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty(dec.q.shape, dtype=torch.bfloat16, device=dev)
+    ws_bytes = sa.sink_attn_decode_workspace_bytes(dec.batch, dec.max_seqlen, dec.num_q_heads, dec.num_kv_heads,
+                                                   64, 16, dec.num_splits)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        sa.sink_attn_prefill(pre.q, pre.k, pre.v, pre.sinks, pre.cu_seqlens, pre.scale, out=out_p,
+                             max_seqlen=pre.max_seqlen)
+
+    def decode():
+        sa.sink_attn_decode(dec.q, dec.k_pages, dec.v_pages, dec.page_table, dec.seqlens_t, dec.sinks, dec.scale,
+                            num_splits=dec.num_splits, out=out_d, max_seqlen=dec.max_seqlen, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+
+    ev = [(_events(), _events()) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)  # first samples land before the timed region
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        (pa, pb), (da, db) = ev[i]
+        pa.record(stream)
+        prefill()
+        pb.record(stream)
+        da.record(stream)
+        decode()
+        db.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    t_pre = [a.elapsed_time(b) for (a, b), _ in ev]
+    t_dec = [a.elapsed_time(b) for _, (a, b) in ev]
+    ms_pre = sum(t_pre) / len(t_pre)
+    ms_dec = sum(t_dec) / len(t_dec)
+    total_ms = sum(t_pre) + sum(t_dec)
+    if dist is not None:
+        t = torch.tensor([total_ms, ms_pre, ms_dec], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, ms_pre, ms_dec = t.tolist()
+
+    flops = workloads.prefill_flops(pre.seqlens, pre.num_q_heads)
+    dbytes = workloads.decode_bytes(dec.seqlens, dec.num_q_heads, dec.num_kv_heads, out_bytes=2)
+    pre_tflops = flops / (ms_pre * 1e-3) / 1e12
+    dec_gbs = dbytes / (ms_dec * 1e-3) / 1e9
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if rank == 0:
+        e2e = _e2e(sa, pre, dec, dev, stream, args)
+
+    if rank != 0:
+        return None
+    peaks, peak_src = _peaks()
+    cpu = _cpu_baseline()
+    line = {
+        "metric": METRIC,
+        "value": round(pre_tflops * world, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "prefill: batch 1, causal, seq 8192, Hq 64, Hkv 8, head_dim 64, sinks N(0,2), scale 1/8; "
+                        "decode: batch 64 x 8192 cached tokens, paged KV (page 16, permuted), num_splits 8",
+            "prefill_out": "bf16", "decode_out": "bf16",
+            "l2": "256 MiB buffer written between timed steps (outside the events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "prefill": {"value": round(pre_tflops * world, 3), "unit": "TFLOP/s", "ms": round(ms_pre, 4),
+                    "flops_per_launch": flops},
+        "decode": {"value": round(dec_gbs * world, 2), "unit": "GB/s", "ms": round(ms_dec, 4),
+                   "bytes_per_launch": dbytes,
+                   "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
+                                "traffic": _traffic("decode_split_kernel", DECODE_SOURCES),
+                                "peak_source": f"{peak_src} (STREAM-style copy)"}},
+        "roofline": {"bound": "tensor", "achieved": round(pre_tflops, 3), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(pre_tflops / peaks["bf16_tflops"], 4),
+                     "traffic": _traffic("prefill_kernel", PREFILL_SOURCES),
+                     "kernel": "prefill_kernel",
+                     "peak_source": f"{peak_src} (cuBLAS bf16 burst)"},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    return line
+
+
+def _e2e(sa, pre, dec, dev, stream, args):
+    """Prefill and decode through the public API from pinned host buffers:
+    each step copies its inputs host->device, runs, and reads the outputs back."""
+    steps = max(3, min(args.steps, 20))
+    h = {n: getattr(pre, n).cpu().pin_memory() for n in ("q", "k", "v", "sinks", "cu_seqlens")}
+    hd = {n: getattr(dec, n).cpu().pin_memory() for n in ("q", "k_pages", "v_pages", "page_table", "seqlens_t",
+                                                           "sinks")}
+    d = {n: torch.empty_like(t, device=dev) for n, t in h.items()}
+    dd = {n: torch.empty_like(t, device=dev) for n, t in hd.items()}
+    out_p = torch.empty(pre.q.shape, dtype=torch.bfloat16, device=dev)
+    out_d = torch.empty(dec.q.shape, dtype=torch.bfloat16, device=dev)
+    host_p = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
+    host_d = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+
+    def step_prefill():
+        for n in h:
+            d[n].copy_(h[n], non_blocking=True)
+        sa.sink_attn_prefill(d["q"], d["k"], d["v"], d["sinks"], d["cu_seqlens"], pre.scale, out=out_p,
+                             max_seqlen=pre.max_seqlen)
+        host_p.copy_(out_p, non_blocking=True)
+
+    def step_decode():
+        for n in hd:
+            dd[n].copy_(hd[n], non_blocking=True)
+        sa.sink_attn_decode(dd["q"], dd["k_pages"], dd["v_pages"], dd["page_table"], dd["seqlens_t"], dd["sinks"],
+                            dec.scale, num_splits=dec.num_splits, out=out_d, max_seqlen=dec.max_seqlen)
+        host_d.copy_(out_d, non_blocking=True)
+
+    res = {}
+    for name, fn in (("prefill", step_prefill), ("decode", step_decode)):
+        fn()
+        torch.cuda.synchronize()
+        a, b = _events()
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / steps
+    flops = workloads.prefill_flops(pre.seqlens, pre.num_q_heads)
+    dbytes = workloads.decode_bytes(dec.seqlens, dec.num_q_heads, dec.num_kv_heads, out_bytes=2)
+    h2d_p = sum(t.numel() * t.element_size() for t in h.values())
+    h2d_d = sum(t.numel() * t.element_size() for t in hd.values())
+    return {"value": round(flops / (res["prefill"] * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d_p, "d2h_bytes_per_step": host_p.numel() * 2,
+            "ms_per_step": round(res["prefill"], 4),
+            "decode": {"value": round(dbytes / (res["decode"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d_d, "d2h_bytes_per_step": host_d.numel() * 2,
+                       "ms_per_step": round(res["decode"], 4)},
+            "steps": steps}
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+PREFILL_SAMPLE_HEADS = 16  # two kv groups of the 8192-token sequence
+
+
+def _oracle_prefill_sample(pre):
+    """Time the oracle on the first PREFILL_SAMPLE_HEADS query heads (their kv
+    heads) of the full 8192-token sequence; returns (seconds, flops)."""
+    import oracle
+    nh = PREFILL_SAMPLE_HEADS
+    nkv = nh // (pre.num_q_heads // pre.num_kv_heads)
+    q, k, v = pre.q[:, :nh].cpu(), pre.k[:, :nkv].cpu(), pre.v[:, :nkv].cpu()
+    t0 = time.perf_counter()
+    oracle.prefill(q, k, v, pre.sinks[:nh].cpu(), pre.cu_seqlens.cpu(), pre.scale)
+    return time.perf_counter() - t0, workloads.prefill_flops(pre.seqlens, nh)
+
+
+def _oracle_decode_sample(dec, seqs=8):
+    import oracle
+    sel = list(range(seqs))
+    t0 = time.perf_counter()
+    oracle.decode(dec.q[sel], dec.k_pages, dec.v_pages, dec.page_table[sel], dec.seqlens_t[sel], dec.sinks,
+                  dec.scale)
+    dt = time.perf_counter() - t0
+    return dt, workloads.decode_bytes([dec.seqlens[i] for i in sel], dec.num_q_heads, dec.num_kv_heads,
+                                      out_bytes=2)
+
+
+def _cpu_baseline():
+    """The float64 oracle, as it stands, on a bounded sample of the workload."""
+    pre = workloads.workload(PREFILL, device="cpu")
+    dt, flops = _oracle_prefill_sample(pre)
+    dec = workloads.make_decode([8192] * 8, seed=2, sink_mode="normal2", scale=0.125, num_splits=8)
+    ddt, dbytes = _oracle_decode_sample(dec)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"prefill of the 8192-token sequence restricted to {PREFILL_SAMPLE_HEADS} of 64 query heads "
+                      f"({flops:.3e} algorithmic flop, {dt:.2f} s)",
+            "decode": {"value": round(dbytes / ddt / 1e9, 4), "unit": "GB/s",
+                       "sample": f"8 sequences x 8192 tokens of the decode batch ({dbytes} algorithmic bytes, "
+                                 f"{ddt:.2f} s)"}}
+
+
+def run_reference(args, dist, rank, world):
+    """The float64 CPU oracle as the reference arm, timed on the host cores."""
+    if rank != 0:
+        return None
+    pre = workloads.workload(PREFILL, device="cpu")
+    dec = workloads.make_decode([8192] * 8, seed=2, sink_mode="normal2", scale=0.125, num_splits=8)
+    steps = args.steps if args.steps <= 3 else 3  # each step is seconds of float64 work
+    warm = min(args.warmup, 1)
+    for _ in range(warm):
+        _oracle_prefill_sample(pre)
+    tp, td, flops, dbytes = 0.0, 0.0, 0, 0
+    for _ in range(steps):
+        dt, flops = _oracle_prefill_sample(pre)
+        tp += dt
+        ddt, dbytes = _oracle_decode_sample(dec)
+        td += ddt
+    val = flops * steps / tp / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(val, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": round((tp + td) / steps * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "prefill: batch 1, causal, seq 8192, Hq 64, Hkv 8, head_dim 64 (sample: "
+                               f"{PREFILL_SAMPLE_HEADS} query heads); decode: 8 of 64 sequences x 8192 tokens"},
+        "decode": {"value": round(dbytes * steps / td / 1e9, 4), "unit": "GB/s"},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                         "sample": f"{PREFILL_SAMPLE_HEADS}/64 query heads of the 8192-token prefill per step"},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        # rank 0 alone times the CPU oracle; other ranks exit without work
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, None, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    dist, rank, world = _dist()
+    if True:
+        line = run_ours(args, dist, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

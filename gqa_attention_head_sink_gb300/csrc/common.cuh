@@ -132,6 +132,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// The two halves of a packed bf16x2 as floats (exact).
+__device__ __forceinline__ float bf16x2_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
 // D += A * B for one m16n8k16 bf16 tile, fp32 accumulate (warp-wide).
 __device__ __forceinline__ void mma_16816_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -238,13 +238,14 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
       pr[nt][2] = fast_exp2(sc[nt][2] - mn_r8);
       pr[nt][3] = fast_exp2(sc[nt][3] - mn_r8);
     }
-    d_r = d_r * al_r + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-    d_r8 = d_r8 * al_r8 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
     uint32_t pa[4];
     pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
     pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
     pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
     pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+    // the normaliser sums the same bf16-rounded weights the PV MMA uses
+    d_r = d_r * al_r + (bf16x2_lo(pa[0]) + bf16x2_hi(pa[0])) + (bf16x2_lo(pa[2]) + bf16x2_hi(pa[2]));
+    d_r8 = d_r8 * al_r8 + (bf16x2_lo(pa[1]) + bf16x2_hi(pa[1])) + (bf16x2_lo(pa[3]) + bf16x2_hi(pa[3]));
     // O = alpha * O + P V over 8 n-tiles of output dims
     const uint32_t vaw[4] = {va.x, va.y, va.z, va.w}, vbw[4] = {vb.x, vb.y, vb.z, vb.w};
     const uint32_t vcw[4] = {vc.x, vc.y, vc.z, vc.w}, vdw[4] = {vd.x, vd.y, vd.z, vd.w};

@@ -31,6 +31,9 @@
 // The running maximum is only raised when a tile's maximum exceeds it by more
 // than 8 (log2 units), so O is rescaled rarely; the final O / d is exact for
 // any reference point, and P stays <= 2^8 which bf16 and fp32 hold easily.
+// d accumulates the bf16-rounded P (the values the PV MMA multiplies), so the
+// rounding of P perturbs the weights of a convex combination of V rows
+// instead of scaling the output.
 #include "common.cuh"
 #include "prefill.h"
 #include "tcgen05.cuh"
@@ -384,9 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             const float p0 = fast_exp2(fmaf(s[half * 64 + 2 * i], sl2, neg_m));
             const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * i + 1], sl2, neg_m));
-            sum0 += p0;
-            sum1 += p1;
             pk[i] = pack_bf16x2(p0, p1);
+            // the normaliser sums the same bf16-rounded weights the PV MMA uses
+            sum0 += bf16x2_lo(pk[i]);
+            sum1 += bf16x2_hi(pk[i]);
           }
           tmem_st32(s_addr + half * 32, pk);
         }
