@@ -156,6 +156,16 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def reduce_max(dist, values, device):
+    """Element-wise maximum of `values` over all ranks (the slowest rank's
+    time is the job's time); identity without a process group."""
+    if dist is None:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _events():
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -224,10 +234,7 @@ def run_ours(args, dist, rank, world):
     ms_pre = sum(t_pre) / len(t_pre)
     ms_dec = sum(t_dec) / len(t_dec)
     total_ms = sum(t_pre) + sum(t_dec)
-    if dist is not None:
-        t = torch.tensor([total_ms, ms_pre, ms_dec], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, ms_pre, ms_dec = t.tolist()
+    total_ms, ms_pre, ms_dec = reduce_max(dist, [total_ms, ms_pre, ms_dec], dev)
 
     flops = workloads.prefill_flops(pre.seqlens, pre.num_q_heads)
     dbytes = workloads.decode_bytes(dec.seqlens, dec.num_q_heads, dec.num_kv_heads, out_bytes=2)

@@ -1,0 +1,59 @@
+"""Multi-process host logic of the benchmark, on CPU with the gloo backend.
+
+The hot path shards into independent replicas (no collective on the data
+path); the only cross-rank step is the timing reduction: every rank reports
+its own elapsed time and the job's time is the slowest rank's.
+"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    try:
+        local = [10.0 * (rank + 1), 1.0 + rank, 5.0 - rank]
+        got = bench.reduce_max(dist, local, torch.device("cpu"))
+        # replicas: every rank builds the same seeded workload independently
+        from gqa_attention_head_sink_gb300 import workloads
+        inp = workloads.make_prefill([40, 7], num_q_heads=4, num_kv_heads=2, seed=3)
+        digest = torch.tensor([float(inp.q.float().sum()), float(inp.sinks.sum())], dtype=torch.float64)
+        gathered = [torch.zeros(2, dtype=torch.float64) for _ in range(world)]
+        dist.all_gather(gathered, digest)
+        q.put((rank, got, [g.tolist() for g in gathered]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_timing_reduction_and_replicas():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, got, gathered in results:
+        assert got == [20.0, 2.0, 5.0]  # slowest rank wins, element-wise
+        assert gathered[0] == gathered[1]  # identical replicas
+
+
+def test_reduce_max_without_process_group():
+    import bench
+    assert bench.reduce_max(None, [1.0, 2.0], torch.device("cpu")) == [1.0, 2.0]
