@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     load,
     sink_attn_decode,
     sink_attn_decode_max_splits,
+    sink_attn_decode_noalloc,
     sink_attn_decode_workspace_bytes,
     sink_attn_get_device_error,
     sink_attn_prefill,

@@ -33,6 +33,8 @@ EXPORTS = {
     "sink_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P]),
     "sink_attn_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                               _P, _SZ, _P]),
+    "sink_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P,
+                                      _P]),
     "sink_attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "sink_attn_decode_max_splits": (_I, [_I, _I, _I, _I, _I]),
     "sink_attn_status_string": (ctypes.c_char_p, [_I]),
@@ -194,4 +196,39 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
                                  OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse), ws_ptr,
                                  ws_bytes, _stream_ptr(stream))
     _check(st, "sink_attn_decode")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def sink_attn_decode_noalloc(q, k_pages, v_pages, page_table, seqlens, sinks, scale: float, num_splits: int = 0,
+                             out=None, out_dtype=torch.float32, lse=None, max_seqlen: Optional[int] = None,
+                             stream=None):
+    """sink_attn_decode without a workspace, for callers that cannot allocate
+    device memory at decode time: the partial states use the library's own
+    16 MiB scratch array.  Pass ``out`` (and ``lse``) preallocated to keep the
+    call itself free of allocations.  Concurrent calls on different streams
+    race on that array."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    B, hq, d = q.shape
+    num_pages, hkv, page_size, _ = k_pages.shape
+    if max_seqlen is None:
+        max_seqlen = int(seqlens.max().item()) if B > 0 else 0
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    _need(out, "out", out.dtype, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    st = load().sink_attn_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                         page_table.shape[1], _ptr(seqlens), B, int(max_seqlen), num_pages,
+                                         _ptr(sinks), hq, hkv, d, page_size, float(scale), int(num_splits), _ptr(out),
+                                         OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse),
+                                         _stream_ptr(stream))
+    _check(st, "sink_attn_decode_noalloc")
     return out

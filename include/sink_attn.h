@@ -145,6 +145,40 @@ size_t sink_attn_decode_workspace_bytes(int batch, int max_seqlen, int num_q_hea
 int sink_attn_decode_max_splits(int batch, int max_seqlen, int num_kv_heads, int page_size,
                                 int num_splits);
 
+/*
+ * sink_attn_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that are not allowed to call cudaMalloc or any other allocator when they
+ * run decode -- code working inside a memory budget fixed in advance, or a
+ * host framework whose decode step forbids allocation.  sink_attn_decode
+ * would otherwise need a caller workspace or allocate one in stream order.
+ *
+ * Same arguments and results as sink_attn_decode, without the workspace:
+ * the per-chunk partial states go to one scratch array owned by the library,
+ * SINK_ATTN_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory that every GPU
+ * loading the library holds until the process exits.  Nothing is allocated.
+ *   - Calls whose partial states need more than that (see
+ *     sink_attn_decode_workspace_bytes) return SINK_ATTN_ERR_UNSUPPORTED and
+ *     enqueue nothing; e.g. batch 64 x 8192 tokens, 64/8 heads, 8 chunks
+ *     needs 8.25 MiB and fits.
+ *   - Every call shares the one array: calls whose kernels overlap on the GPU
+ *     (different streams, or different threads) race and corrupt each other's
+ *     results; serialise them.  The array keeps the last call's contents;
+ *     nothing in it needs clearing between calls.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ */
+#define SINK_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int sink_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                             const int32_t* page_table, int page_table_stride,
+                             const int32_t* seqlens, int batch, int max_seqlen, int num_pages,
+                             const float* sinks, int num_q_heads, int num_kv_heads, int head_dim,
+                             int page_size, float scale, int num_splits,
+                             void* out, int out_dtype, float* lse, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* sink_attn_status_string(int status);
 
