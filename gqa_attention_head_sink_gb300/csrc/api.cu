@@ -100,14 +100,14 @@ int encode_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t ro
 }
 
 // 3-D bf16 tensor map over a packed [tokens, heads, 64] tensor, boxes of
-// 128 tokens x 1 head x 64 dims (one 16 KiB tile of one head), 128-byte swizzle.
-int encode_tokens_heads(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads) {
+// box_tokens tokens x 1 head x 64 dims (one tile of one head), 128-byte swizzle.
+int encode_tokens_heads(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads, uint32_t box_tokens) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   int st = get_encoder(&enc);
   if (st) return st;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
-  cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kPrefillTileRows};
+  cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, box_tokens};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -311,9 +311,9 @@ int sink_attn_prefill(const void* q, const void* k, const void* v, const float* 
     }
   }
   CUtensorMap qmap, kmap, vmap;
-  if ((st = encode_tokens_heads(&qmap, q, total_tokens, num_q_heads))) return st;
-  if ((st = encode_tokens_heads(&kmap, k, total_tokens, num_kv_heads))) return st;
-  if ((st = encode_tokens_heads(&vmap, v, total_tokens, num_kv_heads))) return st;
+  if ((st = encode_tokens_heads(&qmap, q, total_tokens, num_q_heads, kPrefillTileRows))) return st;
+  if ((st = encode_tokens_heads(&kmap, k, total_tokens, num_kv_heads, kPrefillKeyRows))) return st;
+  if ((st = encode_tokens_heads(&vmap, v, total_tokens, num_kv_heads, kPrefillKeyRows))) return st;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
 

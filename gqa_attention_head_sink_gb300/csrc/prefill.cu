@@ -18,16 +18,20 @@
 //     tiles (128-byte swizzle), each slot guarded by a full/empty mbarrier.
 //   * warp 1 (one thread): MMA issuer.  S_t = Q_t K_j^T (M=128, N=128, K=64)
 //     into TMEM, and O_t += P_t V_j (M=128, N=64, K=128) with P_t read from
-//     TMEM (A operand) and V_j from shared memory (MN-major B operand).  Issue
-//     order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1) lets the tensor cores work
-//     on one head while the other head's softmax runs.
+//     TMEM (A operand) and V_j from shared memory (MN-major B operand).
 //   * warps 4..7 / 8..11: softmax of head 0 / head 1, one thread per query row.
-//     Each reads its 128 scores from TMEM, applies the causal mask on the
-//     diagonal tile, updates (m, d), writes P (bf16) back over its scores, and
-//     at the end normalises O by d and stores the row.
+//     Each reads its 128 scores from TMEM and at once hands the S columns back
+//     (so the MMA for the next key tile overlaps this tile's softmax), applies
+//     the causal mask on the diagonal tile, updates (m, d), and writes P (bf16)
+//     to its own TMEM columns once the previous tile's PV has finished with
+//     them; at the end it normalises O by d and stores the row.
 //   * warp 2 allocates / frees the 512 TMEM columns:
-//       S_0 [0,128)  S_1 [128,256)  O_0 [256,320)  O_1 [320,384)
-//     P_t occupies the first 64 columns of S_t (two bf16 per column).
+//       S_0 [0,128)  S_1 [128,256)  O_0 [256,320)  O_1 [320,384)  P_0 [384,448)  P_1 [448,512)
+//     P has two bf16 per column.  Keeping P apart from S means a QK MMA never
+//     waits for the PV MMA reading the previous P.
+// Per head and key tile the only waits are: softmax(j) needs S(j), which the
+// MMA issued when softmax(j-1) released S; it needs PV(j-1) done before it
+// writes P(j) (by then long finished); the MMA needs S released and P written.
 // The running maximum is only raised when a tile's maximum exceeds it by more
 // than 8 (log2 units), so O is rescaled rarely; the final O / d is exact for
 // any reference point, and P stays <= 2^8 which bf16 and fp32 hold easily.
@@ -50,8 +54,9 @@ constexpr int kTileBytes = kTile * kD * 2;  // 16 KiB
 constexpr int kSlots = 8;
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }   // S_t / P_t
+__host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }   // S_t
 __host__ __device__ constexpr uint32_t col_o(int t) { return t ? 320u : 256u; }  // O_t
+__host__ __device__ constexpr uint32_t col_p(int t) { return t ? 448u : 384u; }  // P_t
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
 constexpr float kRescaleThreshold = 8.f;
@@ -60,7 +65,7 @@ constexpr float kRescaleThreshold = 8.f;
 constexpr int kOffQ = 0;                                // 2 Q tiles
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;         // kSlots K/V tiles
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;  // mbarriers
-constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 1;
+constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBar + 256;
 constexpr int kOffSeq = kOffMisc + 64;
 constexpr int kSmemBytes = kOffSeq + 4 * kPrefillMaxBatch * 4 + 1024;
@@ -71,8 +76,10 @@ struct Bars {
   uint64_t* q_empty;
   uint64_t* slot_full;
   uint64_t* slot_empty;
-  uint64_t* s_full;  // [2] MMA -> softmax: scores ready (and, last, O ready)
+  uint64_t* s_full;  // [2] MMA -> softmax: scores of the next tile ready
+  uint64_t* s_free;  // [2] softmax -> MMA: scores read, S columns free
   uint64_t* p_full;  // [2] softmax -> MMA: P written (and O rescaled)
+  uint64_t* o_done;  // [2] MMA -> softmax: a PV (hence every earlier MMA) finished
   uint64_t* drain;
 };
 
@@ -124,6 +131,7 @@ __device__ __forceinline__ bool next_unit(int k, int total, int pairs_per_group,
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const PrefillParams& p,
                                               volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;  // fast path: already complete
   if (*abort_flag) return false;
   if (mbar_wait(bar, parity, p.err, kErrPrefill, p.wait_limit_ns)) return true;
   *abort_flag = 1;
@@ -144,8 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.slot_full = bar_base + 2;
   bars.slot_empty = bars.slot_full + kSlots;
   bars.s_full = bars.slot_empty + kSlots;
-  bars.p_full = bars.s_full + 2;
-  bars.drain = bars.p_full + 2;
+  bars.s_free = bars.s_full + 2;
+  bars.p_full = bars.s_free + 2;
+  bars.o_done = bars.p_full + 2;
+  bars.drain = bars.o_done + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* total_qblocks = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -171,7 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bars.s_full + t, 1);
-      mbar_init(bars.p_full + t, 128);  // every softmax thread of the head arrives
+      mbar_init(bars.s_free + t, 128);  // every softmax thread of the head arrives
+      mbar_init(bars.p_full + t, 128);
+      mbar_init(bars.o_done + t, 1);
     }
     mbar_init(bars.drain, 1);
     *abort_flag = 0;
@@ -211,108 +223,141 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop and waits; one elected lane issues the copies.
+    if (elect_one()) {
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      const uint64_t pol_stream = l2_policy_evict_first();
-      uint32_t ring_i = 0;
-      Unit u;
-      for (int k = 0; next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
-        if (k > 0 && !wait_or_abort(bars.q_empty, (k - 1) & 1, p, abort_flag)) break;
-        const int t0 = seq_start[u.seq] + u.qb * kTile;
-        const int hA = u.g * p.group + 2 * u.pair;
-        const int hB = (2 * u.pair + 1 < p.group) ? hA + 1 : hA;
+    }
+    const uint64_t pol_stream = l2_policy_evict_first();
+    uint32_t ring_i = 0;
+    Unit u;
+    bool ok = true;
+    for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+      if (k > 0 && !(ok = __all_sync(0xffffffffu, wait_or_abort(bars.q_empty, (k - 1) & 1, p, abort_flag)))) break;
+      const int t0 = seq_start[u.seq] + u.qb * kTile;
+      const int hA = u.g * p.group + 2 * u.pair;
+      const int hB = (2 * u.pair + 1 < p.group) ? hA + 1 : hA;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bars.q_full, 2 * kTileBytes);
         tma_load_3d_hint(q_tile[0], &qmap, bars.q_full, 0, hA, t0, pol_stream);
         tma_load_3d_hint(q_tile[1], &qmap, bars.q_full, 0, hB, t0, pol_stream);
-        const int kv0 = seq_start[u.seq];
-        const int n = u.qb + 1;
-        bool ok = true;
-        for (int j = 0; j < n && ok; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const int slot = ring_i % kSlots;
-            if (ring_i >= kSlots && !wait_or_abort(bars.slot_empty + slot, ((ring_i / kSlots) - 1) & 1, p, abort_flag)) {
-              ok = false;
-              break;
-            }
+      }
+      const int kv0 = seq_start[u.seq];
+      const int n = u.qb + 1;
+      for (int j = 0; j < n && ok; ++j) {
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t slot = ring_i % kSlots;
+          if (ring_i >= kSlots &&
+              !(ok = __all_sync(0xffffffffu,
+                                wait_or_abort(bars.slot_empty + slot, ((ring_i / kSlots) - 1) & 1, p, abort_flag))))
+            break;
+          if (elect_one()) {
             mbar_arrive_expect_tx(bars.slot_full + slot, kTileBytes);
-            tma_load_3d(ring + slot * kTileBytes, kv ? &vmap : &kmap, bars.slot_full + slot, 0, u.g,
-                        kv0 + j * kTile);
-            ++ring_i;
+            tma_load_3d(ring + slot * kTileBytes, kv ? &vmap : &kmap, bars.slot_full + slot, 0, u.g, kv0 + j * kTile);
           }
+          ++ring_i;
         }
-        if (!ok) break;
       }
-      if (*abort_flag) {
-        // let copies already in flight land before the CTA can exit
-        for (uint32_t i = ring_i > kSlots ? ring_i - kSlots : 0; i < ring_i; ++i)
-          mbar_wait(bars.slot_full + (i % kSlots), (i / kSlots) & 1, p.err, kErrPrefill, 10000000ull);
-      }
+    }
+    if (__any_sync(0xffffffffu, *abort_flag) && elect_one()) {
+      // let copies already in flight land before the CTA can exit
+      for (uint32_t i = ring_i > kSlots ? ring_i - kSlots : 0; i < ring_i; ++i)
+        mbar_wait(bars.slot_full + (i % kSlots), (i / kSlots) & 1, p.err, kErrPrefill, 10000000ull);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      uint32_t ring_i = 0, pph[2] = {0, 0};
-      const uint64_t dq[2] = {smem_desc_sw128(smem_addr(q_tile[0])), smem_desc_sw128(smem_addr(q_tile[1]))};
-      Unit u;
-      bool ok = true;
-      for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
-        const int n = u.qb + 1;
-        if (!(ok = wait_or_abort(bars.q_full, k & 1, p, abort_flag))) break;
-        // K_0 -> S_0, S_1
-        uint32_t kslot = ring_i % kSlots;
-        if (!(ok = wait_or_abort(bars.slot_full + kslot, (ring_i / kSlots) & 1, p, abort_flag))) break;
+    // The whole warp runs the loop and waits; one elected lane issues each group
+    // of MMAs and commits (warp-uniform operands, see elect_one).
+    uint32_t ring_i = 0, pph[2] = {0, 0}, fph[2] = {0, 0};
+    bool first_qk = true;
+    const uint64_t dq[2] = {smem_desc_sw128(smem_addr(q_tile[0])), smem_desc_sw128(smem_addr(q_tile[1]))};
+    const uint64_t dring = smem_desc_sw128(smem_addr(ring));
+    // descriptor of ring slot i: the start-address field advances 16 KiB >> 4 per slot
+    auto slot_desc = [&](uint32_t i) { return dring + (uint64_t)((i % kSlots) * (kTileBytes >> 4)); };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, abort_flag));
+    };
+    Unit u;
+    bool ok = true;
+    for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+      const int n = u.qb + 1;
+      if (!(ok = wait_all(bars.q_full, k & 1))) break;
+      // K_0 -> S_0, S_1 (each S must first be released by its softmax)
+      if (!(ok = wait_all(bars.slot_full + ring_i % kSlots, (ring_i / kSlots) & 1))) break;
+      const uint64_t dk0 = slot_desc(ring_i);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!first_qk) {
+          if (!(ok = wait_all(bars.s_free + t, fph[t]))) break;
+          fph[t] ^= 1;
+        }
         tc_fence_after();
-        uint64_t dk = smem_desc_sw128(smem_addr(ring + kslot * kTileBytes));
+        if (elect_one()) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) umma_ss(tmem + col_s(t), dq[t] + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);
+          for (int kk = 0; kk < 4; ++kk) umma_ss(tmem + col_s(t), dq[t] + 2 * kk, dk0 + 2 * kk, kIdescQK, kk > 0);
           umma_commit(bars.s_full + t);
         }
-        umma_commit(bars.slot_empty + kslot);
+      }
+      if (!ok) break;
+      first_qk = false;
+      if (elect_one()) {
+        umma_commit(bars.slot_empty + ring_i % kSlots);
         if (n == 1) umma_commit(bars.q_empty);
-        ++ring_i;
-        for (int j = 0; j < n; ++j) {
-          const uint32_t vslot = ring_i % kSlots;
-          if (!(ok = wait_or_abort(bars.slot_full + vslot, (ring_i / kSlots) & 1, p, abort_flag))) break;
-          const uint64_t dv = smem_desc_sw128(smem_addr(ring + vslot * kTileBytes));
-          const bool more = j + 1 < n;
-          if (more) {
-            kslot = (ring_i + 1) % kSlots;
-            if (!(ok = wait_or_abort(bars.slot_full + kslot, ((ring_i + 1) / kSlots) & 1, p, abort_flag))) break;
-            dk = smem_desc_sw128(smem_addr(ring + kslot * kTileBytes));
-          }
+      }
+      ++ring_i;
+      for (int j = 0; j < n; ++j) {
+        const uint32_t vi = ring_i, ki = ring_i + 1;
+        const bool more = j + 1 < n;
+        if (!(ok = wait_all(bars.slot_full + vi % kSlots, (vi / kSlots) & 1))) break;
+        if (more && !(ok = wait_all(bars.slot_full + ki % kSlots, (ki / kSlots) & 1))) break;
+        const uint64_t dv = slot_desc(vi), dk = slot_desc(ki);
+        if (more) {  // scores of tile j+1 as soon as each softmax has read tile j's
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (!(ok = wait_or_abort(bars.p_full + t, pph[t], p, abort_flag))) break;
-            pph[t] ^= 1;
+            if (!(ok = wait_all(bars.s_free + t, fph[t]))) break;
+            fph[t] ^= 1;
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + 128 * kk, kIdescPV, (j > 0) || (kk > 0));
-            if (t == 1) umma_commit(bars.slot_empty + vslot);
-            if (more) {
+            if (elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) umma_ss(tmem + col_s(t), dq[t] + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);
+              umma_commit(bars.s_full + t);
             }
-            umma_commit(bars.s_full + t);  // scores of tile j+1, or the finished O
           }
           if (!ok) break;
-          if (more) {
-            umma_commit(bars.slot_empty + kslot);
+          if (elect_one()) {
+            umma_commit(bars.slot_empty + ki % kSlots);
             if (j + 2 == n) umma_commit(bars.q_empty);
-            ring_i += 2;
-          } else {
-            ring_i += 1;
           }
         }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!(ok = wait_all(bars.p_full + t, pph[t]))) break;
+          pph[t] ^= 1;
+          tc_fence_after();
+          if (elect_one()) {
+            if (j > 0) {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tmem + col_o(t), tmem + col_p(t) + 8 * kk, dv + 128 * kk, kIdescPV, 1);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tmem + col_o(t), tmem + col_p(t) + 8 * kk, dv + 128 * kk, kIdescPV, kk > 0);
+            }
+            umma_commit(bars.o_done + t);
+          }
+        }
+        if (!ok) break;
+        if (elect_one()) umma_commit(bars.slot_empty + vi % kSlots);
+        ring_i += more ? 2 : 1;
       }
-      // every MMA issued by this thread must finish before TMEM is released
-      umma_commit(bars.drain);
-      mbar_wait(bars.drain, 0, p.err, kErrPrefill, p.wait_limit_ns);
     }
+    // every MMA issued by this warp must finish before TMEM is released
+    if (elect_one()) umma_commit(bars.drain);
+    __syncwarp();
+    mbar_wait(bars.drain, 0, p.err, kErrPrefill, p.wait_limit_ns);
   } else if (warp >= 4) {
     // ================================================================ softmax
     const int t = (warp - 4) >> 2;         // which query tile (head of the pair)
@@ -321,8 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + col_s(t);
     const uint32_t o_addr = tmem + lane_off + col_o(t);
+    const uint32_t p_addr = tmem + lane_off + col_p(t);
     const float sl2 = p.scale_log2;
-    uint32_t sph = 0;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    uint32_t sph = 0, oph = 0;
     Unit u;
     bool ok = true;
     for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
@@ -343,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
         tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bars.s_free + t);  // the next tile's QK may overwrite S now
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
@@ -353,19 +402,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 4; c < 124; c += 8) {
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        mx0 = fmax3(mx0, s[124], s[125]);
+        mx1 = fmax3(mx1, s[126], s[127]);
+        const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         const bool need = m_tile > m + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? m_tile : m;
-          const float alpha = fast_exp2(m - m_new);
-          d *= alpha;
-          if (j > 0) {  // O holds tiles 0..j-1 (their MMAs completed before S_j was signalled)
+        const bool any_need = __any_sync(0xffffffffu, need);
+        const float m_new = need ? m_tile : m;
+        const float alpha = fast_exp2(m - m_new);  // 1 unless this row's maximum moved
+        const float2 neg_m2 = make_float2(-m_new, -m_new);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sl2x2, neg_m2);
+          pk[i] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
+          // the normaliser sums the same bf16-rounded weights the PV MMA uses
+          acc[i & 3] = fadd2(acc[i & 3], make_float2(bf16x2_lo(pk[i]), bf16x2_hi(pk[i])));
+        }
+        if (j > 0) {  // PV(j-1) still reads P and accumulates into O until it is done
+          ok = wait_or_abort(bars.o_done + t, oph, p, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          oph ^= 1;
+          tc_fence_after();
+          if (any_need) {
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 16) {
               uint32_t ob[16];
@@ -376,35 +442,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_st16(o_addr + c0, ob);
             }
           }
-          m = m_new;
         }
-        const float neg_m = -m;
-        float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(s[half * 64 + 2 * i], sl2, neg_m));
-            const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * i + 1], sl2, neg_m));
-            pk[i] = pack_bf16x2(p0, p1);
-            // the normaliser sums the same bf16-rounded weights the PV MMA uses
-            sum0 += bf16x2_lo(pk[i]);
-            sum1 += bf16x2_hi(pk[i]);
-          }
-          tmem_st32(s_addr + half * 32, pk);
-        }
+        tmem_st32(p_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(p_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         tmem_st_wait();
-        d += sum0 + sum1;
+        const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+        d = d * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
+        m = m_new;
         tc_fence_before();
         mbar_arrive(bars.p_full + t);
       }
       if (!ok) break;
       // ---- epilogue: wait for the last PV, normalise, store
-      ok = wait_or_abort(bars.s_full + t, sph, p, abort_flag);
+      ok = wait_or_abort(bars.o_done + t, oph, p, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      sph ^= 1;
+      oph ^= 1;
       tc_fence_after();
       uint32_t ob[64];
       tmem_ld32(o_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&ob[0]));

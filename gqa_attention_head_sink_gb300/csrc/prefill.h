@@ -8,7 +8,8 @@
 
 namespace sa {
 
-constexpr int kPrefillTileRows = 128;   // query rows per tile = keys per K/V tile
+constexpr int kPrefillTileRows = 128;   // query rows per tile
+constexpr int kPrefillKeyRows = 128;    // keys per K/V tile
 constexpr int kPrefillMaxBatch = 1024;  // sequences per call (per-CTA schedule table)
 
 struct PrefillParams {
@@ -28,7 +29,8 @@ struct PrefillParams {
 cudaError_t prefill_configure();
 
 // Enqueue the persistent prefill kernel: `grid_ctas` <= number of SMs.
-// qmap / kmap / vmap are 3-D maps over [T, heads, 64] with 128 x 1 x 64 boxes.
+// qmap / kmap / vmap are 3-D maps over [T, heads, 64] with boxes of 128 (q) or
+// 64 (k, v) tokens x 1 head x 64 dims.
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const PrefillParams& p, int num_sms, cudaStream_t stream);
 
