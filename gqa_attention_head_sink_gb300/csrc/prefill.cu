@@ -13,12 +13,14 @@
 //     blocks with the most key tiles first), the heads of one group adjacent so
 //     that concurrently running CTAs read the same K/V from L2, and dealt to
 //     CTAs in a serpentine order.
-//   * warp 0 (one thread): TMA producer.  Loads the two 128x64 Q tiles of a
+//   * warp 0 (elected lane): TMA producer.  Loads the two 128x64 Q tiles of a
 //     unit, then K_0, V_0, K_1, V_1, ... through an 8-slot ring of 16 KiB
 //     tiles (128-byte swizzle), each slot guarded by a full/empty mbarrier.
-//   * warp 1 (one thread): MMA issuer.  S_t = Q_t K_j^T (M=128, N=128, K=64)
-//     into TMEM, and O_t += P_t V_j (M=128, N=64, K=128) with P_t read from
-//     TMEM (A operand) and V_j from shared memory (MN-major B operand).
+//   * warps 1 and 3: MMA issuers for head 0 and head 1.  S_t = Q_t K_j^T
+//     (M=128, N=128, K=64) into TMEM, and O_t += P_t V_j (M=128, N=64, K=128)
+//     with P_t read from TMEM (A operand) and V_j from shared memory (MN-major
+//     B operand).  Each warp runs its loop as a whole warp and issues from an
+//     elect.sync lane: from a lone lane the same MMAs issued ~40% slower.
 //   * warps 4..7 / 8..11: softmax of head 0 / head 1, one thread per query row.
 //     Each reads its 128 scores from TMEM and at once hands the S columns back
 //     (so the MMA for the next key tile overlaps this tile's softmax), applies
@@ -174,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     mbar_init(bars.q_full, 1);
-    mbar_init(bars.q_empty, 1);
+    mbar_init(bars.q_empty, 2);  // released by both MMA warps
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(bars.slot_full + i, 1);
-      mbar_init(bars.slot_empty + i, 1);
+      mbar_init(bars.slot_empty + i, 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bars.s_full + t, 1);
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.p_full + t, 128);
       mbar_init(bars.o_done + t, 1);
     }
-    mbar_init(bars.drain, 1);
+    mbar_init(bars.drain, 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -266,43 +268,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t i = ring_i > kSlots ? ring_i - kSlots : 0; i < ring_i; ++i)
         mbar_wait(bars.slot_full + (i % kSlots), (i / kSlots) & 1, p.err, kErrPrefill, 10000000ull);
     }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    // The whole warp runs the loop and waits; one elected lane issues each group
-    // of MMAs and commits (warp-uniform operands, see elect_one).
-    uint32_t ring_i = 0, pph[2] = {0, 0}, fph[2] = {0, 0};
+  } else if (warp == 1 || warp == 3) {
+    // ================================================================ MMA issuers
+    // Warp 1 issues head 0's MMAs, warp 3 head 1's: each head's S, P and O are
+    // touched only by its own warp's MMAs, whose order tcgen05 keeps; the K/V
+    // slots and the Q tiles are released by a commit from each warp.  The whole
+    // warp runs the loop and waits; one elected lane issues (warp-uniform operands).
+    const int t = warp == 1 ? 0 : 1;
+    uint32_t ring_i = 0, pph = 0, fph = 0;
     bool first_qk = true;
-    const uint64_t dq[2] = {smem_desc_sw128(smem_addr(q_tile[0])), smem_desc_sw128(smem_addr(q_tile[1]))};
+    const uint64_t dq = smem_desc_sw128(smem_addr(q_tile[t]));
     const uint64_t dring = smem_desc_sw128(smem_addr(ring));
     // descriptor of ring slot i: the start-address field advances 16 KiB >> 4 per slot
     auto slot_desc = [&](uint32_t i) { return dring + (uint64_t)((i % kSlots) * (kTileBytes >> 4)); };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, abort_flag));
     };
+    const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t), a_p = tmem + col_p(t);
     Unit u;
     bool ok = true;
     for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
       const int n = u.qb + 1;
       if (!(ok = wait_all(bars.q_full, k & 1))) break;
-      // K_0 -> S_0, S_1 (each S must first be released by its softmax)
+      // K_0 -> S (once the softmax has released S)
       if (!(ok = wait_all(bars.slot_full + ring_i % kSlots, (ring_i / kSlots) & 1))) break;
-      const uint64_t dk0 = slot_desc(ring_i);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (!first_qk) {
-          if (!(ok = wait_all(bars.s_free + t, fph[t]))) break;
-          fph[t] ^= 1;
-        }
-        tc_fence_after();
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) umma_ss(tmem + col_s(t), dq[t] + 2 * kk, dk0 + 2 * kk, kIdescQK, kk > 0);
-          umma_commit(bars.s_full + t);
-        }
+      if (!first_qk) {
+        if (!(ok = wait_all(bars.s_free + t, fph))) break;
+        fph ^= 1;
       }
-      if (!ok) break;
       first_qk = false;
+      tc_fence_after();
       if (elect_one()) {
+        const uint64_t dk0 = slot_desc(ring_i);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) umma_ss(d_s, dq + 2 * kk, dk0 + 2 * kk, kIdescQK, kk > 0);
+        umma_commit(bars.s_full + t);
         umma_commit(bars.slot_empty + ring_i % kSlots);
         if (n == 1) umma_commit(bars.q_empty);
       }
@@ -310,51 +310,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n; ++j) {
         const uint32_t vi = ring_i, ki = ring_i + 1;
         const bool more = j + 1 < n;
-        if (!(ok = wait_all(bars.slot_full + vi % kSlots, (vi / kSlots) & 1))) break;
-        if (more && !(ok = wait_all(bars.slot_full + ki % kSlots, (ki / kSlots) & 1))) break;
-        const uint64_t dv = slot_desc(vi), dk = slot_desc(ki);
-        if (more) {  // scores of tile j+1 as soon as each softmax has read tile j's
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!(ok = wait_all(bars.s_free + t, fph[t]))) break;
-            fph[t] ^= 1;
-            tc_fence_after();
-            if (elect_one()) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) umma_ss(tmem + col_s(t), dq[t] + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);
-              umma_commit(bars.s_full + t);
-            }
-          }
-          if (!ok) break;
+        if (more) {  // scores of tile j+1 as soon as the softmax has read tile j's
+          if (!(ok = wait_all(bars.slot_full + ki % kSlots, (ki / kSlots) & 1))) break;
+          if (!(ok = wait_all(bars.s_free + t, fph))) break;
+          fph ^= 1;
+          tc_fence_after();
           if (elect_one()) {
+            const uint64_t dk = slot_desc(ki);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) umma_ss(d_s, dq + 2 * kk, dk + 2 * kk, kIdescQK, kk > 0);
+            umma_commit(bars.s_full + t);
             umma_commit(bars.slot_empty + ki % kSlots);
             if (j + 2 == n) umma_commit(bars.q_empty);
           }
         }
+        if (!(ok = wait_all(bars.slot_full + vi % kSlots, (vi / kSlots) & 1))) break;
+        if (!(ok = wait_all(bars.p_full + t, pph))) break;
+        pph ^= 1;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dv = slot_desc(vi);
+          if (j > 0) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!(ok = wait_all(bars.p_full + t, pph[t]))) break;
-          pph[t] ^= 1;
-          tc_fence_after();
-          if (elect_one()) {
-            if (j > 0) {
+            for (int kk = 0; kk < 8; ++kk) umma_ts(d_o, a_p + 8 * kk, dv + 128 * kk, kIdescPV, 1);
+          } else {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tmem + col_o(t), tmem + col_p(t) + 8 * kk, dv + 128 * kk, kIdescPV, 1);
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tmem + col_o(t), tmem + col_p(t) + 8 * kk, dv + 128 * kk, kIdescPV, kk > 0);
-            }
-            umma_commit(bars.o_done + t);
+            for (int kk = 0; kk < 8; ++kk) umma_ts(d_o, a_p + 8 * kk, dv + 128 * kk, kIdescPV, kk > 0);
           }
+          umma_commit(bars.o_done + t);
+          umma_commit(bars.slot_empty + vi % kSlots);
         }
-        if (!ok) break;
-        if (elect_one()) umma_commit(bars.slot_empty + vi % kSlots);
         ring_i += more ? 2 : 1;
       }
     }
-    // every MMA issued by this warp must finish before TMEM is released
+    // every MMA issued by these warps must finish before TMEM is released
     if (elect_one()) umma_commit(bars.drain);
     __syncwarp();
     mbar_wait(bars.drain, 0, p.err, kErrPrefill, p.wait_limit_ns);
