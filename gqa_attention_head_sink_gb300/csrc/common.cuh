@@ -167,6 +167,17 @@ __device__ __forceinline__ void regs_decrease() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// acc.x += low bf16 half of pk, acc.y += high half (each widened exactly to
+// fp32, then added in fp32): the mixed-precision add reads the halves in place.
+__device__ __forceinline__ float2 add_bf16x2_f32x2(float2 acc, uint32_t pk) {
+  float2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(pk), "f"(acc.x), "f"(acc.y));
+  return r;
+}
+
 // The two halves of a packed bf16x2 as floats (exact).
 __device__ __forceinline__ float bf16x2_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }

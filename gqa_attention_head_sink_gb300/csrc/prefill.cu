@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sl2x2, neg_m2);
           pk[i] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
           // the normaliser sums the same bf16-rounded weights the PV MMA uses
-          acc[i & 3] = fadd2(acc[i & 3], make_float2(bf16x2_lo(pk[i]), bf16x2_hi(pk[i])));
+          acc[i & 3] = add_bf16x2_f32x2(acc[i & 3], pk[i]);
         }
         if (j > 0) {  // PV(j-1) still reads P and accumulates into O until it is done
           ok = wait_or_abort(bars.o_done + t, oph, p, abort_flag);
