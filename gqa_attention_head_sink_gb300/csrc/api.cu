@@ -37,6 +37,7 @@ constexpr int kMaxSplitPages = 128;
 std::mutex g_mutex;
 unsigned* g_err_ptr[kMaxDevices] = {};
 bool g_prefill_attr_set[kMaxDevices] = {};
+bool g_decode_attr_set[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -235,6 +236,13 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
   if (st) return st;
   unsigned* err;
   if ((st = error_word(dev, &err))) return st;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_decode_attr_set[dev]) {
+      if (decode_configure() != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+      g_decode_attr_set[dev] = true;
+    }
+  }
   const uint64_t rows = (uint64_t)num_pages * num_kv_heads * kPageSize;
   CUtensorMap kmap, vmap;
   if ((st = encode_rows64(&kmap, k_pages, rows, kHeadDim * 2, kPageSize))) return st;

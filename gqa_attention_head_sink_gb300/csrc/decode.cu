@@ -59,7 +59,9 @@ __device__ __forceinline__ void chunk_range(const DecodeParams& p, int L, int s,
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
+// Four CTAs per SM (96 registers a thread) keep enough page copies in flight
+// to approach the HBM bandwidth.
+__global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 const DecodeParams p) {
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -378,6 +380,14 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
 }
 
 size_t decode_smem_bytes() { return kRingBytes + 2 * kStages * 8 + 16 + 1024; }
+
+cudaError_t decode_configure() {
+  // Prefer shared memory over L1 so four CTAs' rings fit on an SM.
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)decode_smem_bytes());
+}
 int decode_threads() { return kThreads; }
 
 }  // namespace sa

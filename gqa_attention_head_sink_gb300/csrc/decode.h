@@ -46,6 +46,9 @@ __global__ void decode_split_kernel(const __grid_constant__ CUtensorMap kmap, co
 __global__ void decode_merge_kernel(const DecodeParams p);
 
 size_t decode_smem_bytes();
+
+// One-time per-device kernel attributes (shared-memory carveout, size).
+cudaError_t decode_configure();
 int decode_threads();
 
 // Enqueue the chunk kernel and, when chunks are merged, the merge kernel.
