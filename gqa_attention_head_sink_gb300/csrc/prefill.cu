@@ -374,10 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sph ^= 1;
         tc_fence_after();
         uint32_t sr[128];
-        tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-        tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_ld128(s_addr, sr);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(bars.s_free + t);  // the next tile's QK may overwrite S now
@@ -432,8 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tmem_st32(p_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(p_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_st64(p_addr, pk);
         tmem_st_wait();
         const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
         d = d * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
@@ -449,8 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       oph ^= 1;
       tc_fence_after();
       uint32_t ob[64];
-      tmem_ld32(o_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&ob[0]));
-      tmem_ld32(o_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&ob[32]));
+      tmem_ld64(o_addr, ob);
       tmem_ld_wait();
       const int row_tok = u.qb * kTile + r;
       const int tok = seq_start[u.seq] + row_tok;  // checked against T too: cu_seqlens is not trusted
