@@ -52,6 +52,17 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
+// Failure-path testing only: SINK_ATTN_DEBUG_WITHHOLD_COPIES=1 makes the TMA
+// producers issue nothing, so every bounded wait gives up and the call reports
+// SINK_ATTN_ERR_TIMEOUT through sink_attn_get_device_error().  Read once.
+int withhold_copies() {
+  static int v = [] {
+    const char* s = std::getenv("SINK_ATTN_DEBUG_WITHHOLD_COPIES");
+    return (s && s[0] == '1') ? 1 : 0;
+  }();
+  return v;
+}
+
 int current_device(int* dev) {
   if (cudaGetDevice(dev) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
   if (*dev < 0 || *dev >= kMaxDevices) return SINK_ATTN_ERR_UNSUPPORTED;
@@ -283,6 +294,7 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
   p.out_f32 = out_dtype == SINK_ATTN_OUT_F32;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
+  p.withhold_copies = withhold_copies();
   cudaError_t e = launch_decode(kmap, vmap, p, s);
   if (owned) cudaFreeAsync(ws, s);
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
@@ -340,6 +352,7 @@ int sink_attn_prefill(const void* q, const void* k, const void* v, const float* 
   p.out_f32 = out_dtype == SINK_ATTN_OUT_F32;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
+  p.withhold_copies = withhold_copies();
   cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }

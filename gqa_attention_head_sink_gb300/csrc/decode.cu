@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
           if (i >= kStages) ok = mbar_wait(&empty[st], ((i / kStages) - 1) & 1, p.err, kErrDecodeEmpty, p.wait_limit_ns);
           if (!ok || *abort_flag) {
             *abort_flag = 1;
-          } else {
+          } else if (!p.withhold_copies) {
             uint8_t* dst = smem + st * kStageBytes;
             const int y = (page * p.hkv + g) * kPage;
             mbar_arrive_expect_tx(&full[st], kStageBytes);

@@ -27,6 +27,7 @@ struct DecodeParams {
   int out_f32;
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
+  int withhold_copies;  // failure-path test: the producer issues no copies, so the waits time out
 };
 
 // Number of chunks sequence with `npages` pages is cut into.  Every chunk is

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t0 = seq_start[u.seq] + u.qb * kTile;
       const int hA = u.g * p.group + 2 * u.pair;
       const int hB = (2 * u.pair + 1 < p.group) ? hA + 1 : hA;
-      if (elect_one()) {
+      if (!p.withhold_copies && elect_one()) {
         mbar_arrive_expect_tx(bars.q_full, 2 * kTileBytes);
         tma_load_3d_hint(q_tile[0], &qmap, bars.q_full, 0, hA, t0, pol_stream);
         tma_load_3d_hint(q_tile[1], &qmap, bars.q_full, 0, hB, t0, pol_stream);
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               !(ok = __all_sync(0xffffffffu,
                                 wait_or_abort(bars.slot_empty + slot, ((ring_i / kSlots) - 1) & 1, p, abort_flag))))
             break;
-          if (elect_one()) {
+          if (!p.withhold_copies && elect_one()) {
             mbar_arrive_expect_tx(bars.slot_full + slot, kTileBytes);
             tma_load_3d(ring + slot * kTileBytes, kv ? &vmap : &kmap, bars.slot_full + slot, 0, u.g, kv0 + j * kTile);
           }

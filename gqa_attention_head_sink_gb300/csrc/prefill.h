@@ -23,6 +23,7 @@ struct PrefillParams {
   int out_f32;
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
+  int withhold_copies;  // failure-path test: the producer issues no copies, so the waits time out
 };
 
 // One-time per-device kernel attributes (dynamic shared memory size).
