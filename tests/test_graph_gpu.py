@@ -1,0 +1,76 @@
+"""Decode and prefill captured in a CUDA graph and replayed on new inputs.
+
+A serving loop replays one captured decode step per token.  The decode plans
+its chunks on the device from the lengths in `seqlens`; the host only passes
+an upper bound (max_seqlen) that fixes the grid.  So a graph captured once
+(with a caller-owned workspace, outputs preallocated, bound fixed) must give,
+after the inputs are overwritten in place, exactly what a direct call on the
+new inputs gives -- including new lengths up to the bound.  The first call on
+a device does one-time set-up and must happen before capture.
+"""
+import pytest
+import torch
+
+import gqa_attention_head_sink_gb300 as sa
+from gqa_attention_head_sink_gb300 import build, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    build.build()
+    sa.load()
+
+
+def test_decode_graph_replay_follows_new_lengths_and_data():
+    bound = 4096
+    d = workloads.make_decode([bound, bound, bound], seed=41, sink_mode="mixed", num_splits=0, device="cuda")
+    need = sa.sink_attn_decode_workspace_bytes(d.batch, bound, 64, 8, 64, 16, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.empty((d.batch, 64, 64), dtype=torch.float32, device="cuda")
+
+    def step():
+        sa.sink_attn_decode(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale, num_splits=0,
+                            out=out, max_seqlen=bound, workspace=ws)
+
+    step()  # one-time set-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    # overwrite the inputs in place: other lengths (within the bound), new query and cache contents
+    g = torch.Generator(device="cuda").manual_seed(7)
+    d.seqlens_t.copy_(torch.tensor([17, 4096, 2049], dtype=torch.int32, device="cuda"))
+    d.q.copy_(torch.randn(d.q.shape, generator=g, device="cuda").to(torch.bfloat16))
+    d.k_pages.copy_(torch.randn(d.k_pages.shape, generator=g, device="cuda").to(torch.bfloat16))
+    graph.replay()
+    torch.cuda.synchronize()
+    want = sa.sink_attn_decode(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale, num_splits=0,
+                               max_seqlen=bound, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want)
+    assert sa.sink_attn_get_device_error() == 0
+
+
+def test_prefill_graph_replay_follows_new_data():
+    p = workloads.make_prefill([700, 129, 1000], num_q_heads=16, num_kv_heads=2, seed=42, device="cuda")
+    out = torch.empty(p.q.shape, dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        sa.sink_attn_prefill(p.q, p.k, p.v, p.sinks, p.cu_seqlens, p.scale, out=out, max_seqlen=p.max_seqlen)
+
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    g = torch.Generator(device="cuda").manual_seed(8)
+    p.q.copy_(torch.randn(p.q.shape, generator=g, device="cuda").to(torch.bfloat16))
+    p.v.copy_(torch.randn(p.v.shape, generator=g, device="cuda").to(torch.bfloat16))
+    graph.replay()
+    torch.cuda.synchronize()
+    want = sa.sink_attn_prefill(p.q, p.k, p.v, p.sinks, p.cu_seqlens, p.scale, out_dtype=torch.bfloat16,
+                                max_seqlen=p.max_seqlen)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want)
