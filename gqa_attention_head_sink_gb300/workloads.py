@@ -67,7 +67,7 @@ class PrefillInputs:
 
 @dataclasses.dataclass
 class DecodeInputs:
-    q: torch.Tensor            # [B, Hq, D] bf16
+    q: torch.Tensor            # [B, Hq, D] bf16, or [B, n, Hq, D] for n new tokens per sequence
     k_pages: torch.Tensor      # [num_pages, Hkv, page_size, D] bf16
     v_pages: torch.Tensor      # [num_pages, Hkv, page_size, D] bf16
     page_table: torch.Tensor   # [B, stride] int32, unused entries -1
@@ -88,7 +88,12 @@ class DecodeInputs:
 
     @property
     def num_q_heads(self) -> int:
-        return self.q.shape[1]
+        return self.q.shape[-2]
+
+    @property
+    def q_len(self) -> int:
+        """New query tokens per sequence (1 for a [B, Hq, D] query)."""
+        return self.q.shape[1] if self.q.dim() == 4 else 1
 
     @property
     def num_kv_heads(self) -> int:
@@ -151,8 +156,11 @@ def make_prefill(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, see
 
 def make_decode(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, seed=0,
                 sink_mode="normal2", scale: Optional[float] = None, num_splits=0,
-                page_size=PAGE_SIZE, spare_pages=0, poison=False, device="cpu") -> DecodeInputs:
-    """Paged decode inputs: one bf16 query per sequence, KV pool in pages of
+                page_size=PAGE_SIZE, spare_pages=0, poison=False, q_len: Optional[int] = None,
+                device="cpu") -> DecodeInputs:
+    """Paged decode inputs: one bf16 query per sequence (q [B, Hq, D]), or
+    ``q_len`` new query tokens per sequence (q [B, q_len, Hq, D]: the last
+    q_len tokens of each sequence's cache), KV pool in pages of
     ``page_size`` tokens laid out [num_pages, Hkv, page_size, D], and a page
     table that maps each sequence's logical pages to a random permutation of
     the pool.  ``spare_pages`` adds pool pages that no sequence owns.  With
@@ -165,7 +173,8 @@ def make_decode(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, seed
     num_pages = max(1, used + int(spare_pages))
     gen = _generator(device, seed)
     sinks = draw_sinks(num_q_heads, sink_mode, gen, device)
-    q = _randn_bf16((B, num_q_heads, head_dim), gen, device)
+    q_shape = (B, num_q_heads, head_dim) if q_len is None else (B, int(q_len), num_q_heads, head_dim)
+    q = _randn_bf16(q_shape, gen, device)
     k_pages = _randn_bf16((num_pages, num_kv_heads, page_size, head_dim), gen, device)
     v_pages = _randn_bf16((num_pages, num_kv_heads, page_size, head_dim), gen, device)
     perm = torch.randperm(num_pages, generator=gen, device=device).to(torch.int32)
@@ -263,12 +272,12 @@ def prefill_flops(seqlens, num_q_heads, head_dim=HEAD_DIM) -> int:
 
 
 def decode_bytes(seqlens, num_q_heads, num_kv_heads, head_dim=HEAD_DIM, out_bytes=2,
-                 page_size=PAGE_SIZE) -> int:
+                 page_size=PAGE_SIZE, q_len=1) -> int:
     """Bytes a decode step must move at least once: K and V of every valid
-    token (once per kv head), the queries, the outputs, the used page-table
-    entries and the lengths."""
+    token (once per kv head), the queries (q_len per sequence), the outputs,
+    the used page-table entries and the lengths."""
     kv = sum(seqlens) * num_kv_heads * head_dim * 2 * 2
-    q = len(seqlens) * num_q_heads * head_dim * 2
-    o = len(seqlens) * num_q_heads * head_dim * out_bytes
+    q = len(seqlens) * q_len * num_q_heads * head_dim * 2
+    o = len(seqlens) * q_len * num_q_heads * head_dim * out_bytes
     table = sum((L + page_size - 1) // page_size for L in seqlens) * 4
     return kv + q + o + table + 4 * len(seqlens)

@@ -7,8 +7,10 @@ the CUDA library.
 from .sink_attention import (  # noqa: F401
     attend_rows,
     decode,
+    decode_multi,
     gather_paged_kv,
     online_split_merge,
+    paged_attention,
     prefill,
     prefill_rows,
     sink_softmax_rows,

@@ -30,6 +30,11 @@ design notes of this repository):
   * Prefill is causal with query length equal to key length: query i of a
     sequence sees keys 0..i of the same sequence.
   * Decode: the single query of sequence b sees all seqlens[b] cached keys.
+  * Several new queries per sequence against a paged cache (multi-token
+    decode for speculative / multi-token-prediction drafts, and chunked
+    prefill): the n queries are the last n tokens of the cache, so query t
+    (0-based) sits at position seqlens[b] - n + t and sees keys 0..that
+    position.  The causal mask is aligned to the end of the key range.
   * Degenerate rows: with no key and sink = -inf the output is defined as 0;
     sink = +inf is taken as its limit (output 0).
 
@@ -55,6 +60,8 @@ __all__ = [
     "decode",
     "gather_paged_kv",
     "online_split_merge",
+    "paged_attention",
+    "decode_multi",
 ]
 
 # Rows of the score matrix computed at once, only to bound memory (the result
@@ -299,3 +306,63 @@ def online_split_merge(s_row, sink: float, v, cuts):
         total_d += dd * w
         total += acc * w
     return total / total_d
+
+
+def paged_attention(q, k_pages, v_pages, page_table, seqlens, cu_seqlens_q, sinks, scale: float,
+                    page_size: int = 16):
+    """Queries that are the last tokens of their sequences, against a paged
+    KV cache (definition, float64).
+
+    q : [Tq, Hq, D] packed over sequences by cu_seqlens_q [B+1];
+    k_pages, v_pages : [num_pages, Hkv, page_size, D]; page_table : [B, stride];
+    seqlens : [B] cached tokens per sequence, the new ones included.
+    Sequence b has n_b = cu_q[b+1] - cu_q[b] queries; query t of it sits at
+    position seqlens[b] - n_b + t and sees keys 0..that position (causal, the
+    mask aligned to the end of the cache; a query whose position is negative
+    sees no key).  n_b = 1 is plain decode; n_b = seqlens[b] is causal prefill
+    of the whole sequence.  Returns (out [Tq, Hq, D], lse [Tq, Hq]).
+    """
+    q = _as_f64(q)
+    sinks = _as_f64(sinks)
+    table = _as_int(page_table)
+    lens = _as_int(seqlens)
+    cu = _as_int(cu_seqlens_q)
+    Tq, hq, d = q.shape
+    hkv = k_pages.shape[1]
+    group = hq // hkv
+    out = np.zeros((Tq, hq, d))
+    lse = np.full((Tq, hq), -math.inf)
+    for b in range(len(cu) - 1):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        n, L = t1 - t0, int(lens[b])
+        if n == 0:
+            continue
+        kk = gather_paged_kv(k_pages, table[b], L, page_size)
+        vv = gather_paged_kv(v_pages, table[b], L, page_size)
+        pos = L - n + np.arange(n)  # absolute position of each query
+        mask = np.arange(L)[None, :] <= pos[:, None]
+        for h in range(hq):
+            g = h // group
+            for r0 in range(0, n, _ROW_BLOCK):
+                r1 = min(n, r0 + _ROW_BLOCK)
+                s = scale * (q[t0 + r0:t0 + r1, h, :] @ kk[:, g, :].T)
+                s = np.where(mask[r0:r1], s, -math.inf)
+                o, l = attend_rows(s, float(sinks[h]), vv[:, g, :])
+                out[t0 + r0:t0 + r1, h] = o
+                lse[t0 + r0:t0 + r1, h] = l
+    return out, lse
+
+
+def decode_multi(q, k_pages, v_pages, page_table, seqlens, sinks, scale: float, page_size: int = 16):
+    """Multi-token decode: the same number of new queries for every sequence.
+
+    q : [B, n, Hq, D], the last n tokens of each sequence's cache (query t at
+    position seqlens[b] - n + t, causal among the new tokens).  Returns
+    (out [B, n, Hq, D], lse [B, n, Hq]); ``paged_attention`` with n queries
+    per sequence.
+    """
+    B, n, hq, d = q.shape
+    cu = np.arange(B + 1, dtype=np.int64) * n
+    qp = q.reshape(B * n, hq, d)
+    out, lse = paged_attention(qp, k_pages, v_pages, page_table, seqlens, cu, sinks, scale, page_size)
+    return out.reshape(B, n, hq, d), lse.reshape(B, n, hq)

@@ -15,7 +15,12 @@ one test:
     sink drives the output to 0 monotonically; the pages' online algorithm
     split at any cut points (sink only in the first chunk) gives the direct
     result; GQA equals MHA with each kv head repeated for its group; decode
-    equals the last causal prefill row; page permutations do not matter.
+    equals the last causal prefill row; page permutations do not matter;
+  * several new queries per sequence against the paged cache: 50-digit brute
+    force reading keys straight from the pages, torch SDPA with an explicit
+    mask aligned to the end of the cache, one query = decode, every token new
+    = causal prefill, and queries placed before the cache start see only the
+    sink.
 
 Source of the definition: Perplexity, "GPT-OSS on day 0", section
 "Sink Attention" and the model overview's attention bullet.
@@ -315,3 +320,118 @@ def test_prefill_rows_agrees_with_full_definition():
     o2, l2 = oracle.prefill_rows(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, inp.scale, toks, heads)
     np.testing.assert_allclose(o2, out[toks][:, heads], rtol=0, atol=1e-14)
     np.testing.assert_allclose(l2, lse[toks][:, heads], rtol=0, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# several new queries per sequence against the paged cache
+# --------------------------------------------------------------------------
+def _brute_paged(q, k_pages, v_pages, table, lens, cu_q, sinks, scale, P):
+    """50-digit brute force; keys fetched straight from the pages, query t of
+    sequence b at absolute position lens[b] - n_b + t sees keys 0..position."""
+    import mpmath
+    mpmath.mp.dps = 50
+    Tq, hq, d = q.shape
+    hkv = k_pages.shape[1]
+    out = np.zeros((Tq, hq, d))
+    lse = np.zeros((Tq, hq))
+    for b in range(len(lens)):
+        n = cu_q[b + 1] - cu_q[b]
+        for t in range(n):
+            pos = lens[b] - n + t
+            for h in range(hq):
+                g = h * hkv // hq
+                terms, vals = [], []
+                for j in range(0, pos + 1):
+                    page = table[b][j // P]
+                    dot = mpmath.mpf(0)
+                    for e in range(d):
+                        dot += mpmath.mpf(float(q[cu_q[b] + t, h, e])) * mpmath.mpf(float(k_pages[page, g, j % P, e]))
+                    terms.append(mpmath.e ** (mpmath.mpf(scale) * dot))
+                    vals.append([mpmath.mpf(float(v_pages[page, g, j % P, e])) for e in range(d)])
+                z = sum(terms) + (mpmath.e ** mpmath.mpf(float(sinks[h])) if sinks[h] != -math.inf else 0)
+                for e in range(d):
+                    out[cu_q[b] + t, h, e] = float(sum(w * vv[e] for w, vv in zip(terms, vals)) / z) if z else 0.0
+                lse[cu_q[b] + t, h] = float(mpmath.log(z)) if z else -math.inf
+    return out, lse
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_paged_attention_matches_brute_force(seed):
+    rng = np.random.default_rng(200 + seed)
+    P, hq, hkv, d = 2, 4, 2, 3
+    lens = [3, 0, 5, 2, 4]
+    n_q = [2, 1, 3, 4, 4]  # the fourth sequence has more queries than cached tokens
+    cu_q = np.concatenate([[0], np.cumsum(n_q)]).astype(np.int64)
+    pages = 16
+    k_pages, v_pages = rng.normal(size=(pages, hkv, P, d)), rng.normal(size=(pages, hkv, P, d))
+    table = rng.permutation(pages)[:15].reshape(5, 3)
+    q = rng.normal(size=(int(cu_q[-1]), hq, d))
+    sinks = np.array([0.3, -math.inf, 2.5, -1.1])
+    out, lse = oracle.paged_attention(q, k_pages, v_pages, table, np.array(lens), cu_q, sinks, 0.8, page_size=P)
+    bo, bl = _brute_paged(q, k_pages, v_pages, table, lens, cu_q, sinks, 0.8, P)
+    np.testing.assert_allclose(out, bo, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, bl, rtol=0, atol=1e-13)
+
+
+def _gather_torch(pages, row, L, P):
+    """[L, Hkv, D] keys of one sequence by index arithmetic on the pool."""
+    j = torch.arange(L)
+    return pages[torch.as_tensor(row).long()[j // P], :, j % P, :]
+
+
+def test_decode_multi_no_sink_is_sdpa_with_bottom_right_mask():
+    inp = workloads.make_decode([40, 17, 64, 5], num_q_heads=8, num_kv_heads=2, head_dim=16, seed=21,
+                                sink_mode="neginf", q_len=5, spare_pages=2, poison=True)
+    out, _ = oracle.decode_multi(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.seqlens_t, inp.sinks,
+                                 inp.scale)
+    assert np.all(np.isfinite(out))
+    for b, L in enumerate(inp.seqlens):
+        n = 5
+        kk = _gather_torch(inp.k_pages, inp.page_table[b], L, 16).double()
+        vv = _gather_torch(inp.v_pages, inp.page_table[b], L, 16).double()
+        kk, vv = kk.repeat_interleave(4, dim=1), vv.repeat_interleave(4, dim=1)
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            inp.q[b].double().permute(1, 0, 2), kk.permute(1, 0, 2), vv.permute(1, 0, 2), attn_mask=mask,
+            scale=inp.scale)
+        np.testing.assert_allclose(out[b], o.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_decode_multi_one_token_is_decode_and_last_token_sees_all():
+    d1 = workloads.make_decode([37, 16, 1, 0, 50], num_q_heads=4, num_kv_heads=2, head_dim=8, seed=22,
+                               sink_mode="normal2", q_len=1)
+    out, lse = oracle.decode_multi(d1.q, d1.k_pages, d1.v_pages, d1.page_table, d1.seqlens_t, d1.sinks, d1.scale)
+    o1, l1 = oracle.decode(d1.q[:, 0], d1.k_pages, d1.v_pages, d1.page_table, d1.seqlens_t, d1.sinks, d1.scale)
+    np.testing.assert_allclose(out[:, 0], o1, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[:, 0], l1, rtol=0, atol=1e-14)
+    d4 = workloads.make_decode([37, 16, 50], num_q_heads=4, num_kv_heads=2, head_dim=8, seed=23,
+                               sink_mode="normal2", q_len=4)
+    out, lse = oracle.decode_multi(d4.q, d4.k_pages, d4.v_pages, d4.page_table, d4.seqlens_t, d4.sinks, d4.scale)
+    o1, l1 = oracle.decode(d4.q[:, 3], d4.k_pages, d4.v_pages, d4.page_table, d4.seqlens_t, d4.sinks, d4.scale)
+    np.testing.assert_allclose(out[:, 3], o1, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[:, 3], l1, rtol=0, atol=1e-14)
+
+
+def test_paged_attention_whole_sequence_is_causal_prefill():
+    # every token new (n = L): the mask aligned to the end is the prefill mask
+    lens = [33, 1, 20]
+    d = workloads.make_decode(lens, num_q_heads=6, num_kv_heads=3, head_dim=8, seed=24, sink_mode="mixed")
+    rng = np.random.default_rng(25)
+    q = rng.normal(size=(sum(lens), 6, 8))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    out, lse = oracle.paged_attention(q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, cu, d.sinks, 0.3)
+    kk = np.concatenate([oracle.gather_paged_kv(d.k_pages, d.page_table[b], L, 16) for b, L in enumerate(lens)])
+    vv = np.concatenate([oracle.gather_paged_kv(d.v_pages, d.page_table[b], L, 16) for b, L in enumerate(lens)])
+    o2, l2 = oracle.prefill(q, kk, vv, d.sinks, cu, 0.3)
+    np.testing.assert_allclose(out, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, l2, rtol=0, atol=1e-13)
+
+
+def test_queries_before_the_cache_start_see_only_the_sink():
+    d = workloads.make_decode([2], num_q_heads=4, num_kv_heads=1, head_dim=8, seed=26, sink_mode="mixed", q_len=5)
+    out, lse = oracle.decode_multi(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale)
+    sinks = d.sinks.numpy().astype(np.float64)
+    # queries 0..2 sit at positions -3..-1: no key, so out = 0 and lse = sink
+    np.testing.assert_array_equal(out[0, :3], 0.0)
+    np.testing.assert_array_equal(lse[0, :3], np.broadcast_to(sinks, (3, 4)))
+    assert np.abs(out[0, 3:]).max() > 0
