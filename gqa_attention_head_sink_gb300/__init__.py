@@ -1,7 +1,8 @@
 """GB300-native grouped-query attention with a per-head attention sink.
 
 Python face of the C-ABI library libsink_attn.so (see include/sink_attn.h):
-causal variable-length prefill and split-KV paged decode.  The functions only
+causal variable-length prefill, split-KV paged decode, and multi-token
+decode (several new tokens per sequence against the paged cache).  The functions only
 marshal torch tensors into the C calls; all the arithmetic runs in the CUDA
 kernels, and a missing library is an error, never a fallback.
 """
@@ -12,6 +13,8 @@ from .binding import (  # noqa: F401
     load,
     sink_attn_decode,
     sink_attn_decode_max_splits,
+    sink_attn_decode_multi,
+    sink_attn_decode_multi_workspace_bytes,
     sink_attn_decode_noalloc,
     sink_attn_decode_workspace_bytes,
     sink_attn_get_device_error,

@@ -35,7 +35,10 @@ EXPORTS = {
                               _P, _SZ, _P]),
     "sink_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                                       _P]),
+    "sink_attn_decode_multi": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I,
+                                    _P, _P, _SZ, _P]),
     "sink_attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "sink_attn_decode_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "sink_attn_decode_max_splits": (_I, [_I, _I, _I, _I, _I]),
     "sink_attn_status_string": (ctypes.c_char_p, [_I]),
     "sink_attn_get_device_error": (_I, [_P]),
@@ -155,6 +158,16 @@ def sink_attn_decode_workspace_bytes(batch: int, max_seqlen: int, num_q_heads: i
     return n
 
 
+def sink_attn_decode_multi_workspace_bytes(batch: int, q_len: int, max_seqlen: int, num_q_heads: int,
+                                           num_kv_heads: int, head_dim: int = 64, page_size: int = 16,
+                                           num_splits: int = 0) -> int:
+    n = load().sink_attn_decode_multi_workspace_bytes(batch, q_len, max_seqlen, num_q_heads, num_kv_heads,
+                                                      head_dim, page_size, num_splits)
+    if n == ctypes.c_size_t(-1).value:
+        raise SinkAttnError(1, "sink_attn_decode_multi_workspace_bytes")
+    return n
+
+
 def sink_attn_decode_max_splits(batch: int, max_seqlen: int, num_kv_heads: int, page_size: int = 16,
                                 num_splits: int = 0) -> int:
     return load().sink_attn_decode_max_splits(batch, max_seqlen, num_kv_heads, page_size, num_splits)
@@ -196,6 +209,45 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
                                  OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse), ws_ptr,
                                  ws_bytes, _stream_ptr(stream))
     _check(st, "sink_attn_decode")
+    return out
+
+
+def sink_attn_decode_multi(q, k_pages, v_pages, page_table, seqlens, sinks, scale: float, num_splits: int = 0,
+                           out=None, out_dtype=torch.float32, lse=None, max_seqlen: Optional[int] = None,
+                           workspace=None, stream=None):
+    """Multi-token decode.  q [B,n,Hq,64] bf16 holds the last n tokens of each
+    sequence's cache (token t at position seqlens[b] - n + t, causal among the
+    new tokens); the other arguments are those of sink_attn_decode
+    (workspace: sink_attn_decode_multi_workspace_bytes(...)).  Returns out
+    [B,n,Hq,64]."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    B, n, hq, d = q.shape
+    num_pages, hkv, page_size, d2 = k_pages.shape
+    if v_pages.shape != k_pages.shape or d2 != d:
+        raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
+    if page_table.shape[0] != B or seqlens.shape[0] != B:
+        raise ValueError("page_table and seqlens need one row per sequence")
+    if max_seqlen is None:
+        max_seqlen = int(seqlens.max().item()) if B > 0 else 0
+    if out is None:
+        out = torch.empty((B, n, hq, d), dtype=out_dtype, device=q.device)
+    _need(out, "out", out.dtype, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = load().sink_attn_decode_multi(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                       page_table.shape[1], _ptr(seqlens), B, n, int(max_seqlen), num_pages,
+                                       _ptr(sinks), hq, hkv, d, page_size, float(scale), int(num_splits), _ptr(out),
+                                       OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse), ws_ptr,
+                                       ws_bytes, _stream_ptr(stream))
+    _check(st, "sink_attn_decode_multi")
     return out
 
 

@@ -27,6 +27,7 @@ constexpr int kHeadDim = 64;
 constexpr int kPageSize = 16;
 constexpr int kMaxSplits = 256;
 constexpr int kMaxGroupDecode = 16;
+constexpr int kMaxDecodeRows = 64;  // query rows per kv head in decode: group * new tokens
 constexpr int kMaxDevices = 64;
 // Chunk sizing for num_splits == 0: aim for about this many CTAs in the
 // chunk grid (8 per SM of a 152-SM GB300) with 16..128 pages per chunk.
@@ -134,8 +135,9 @@ struct DecodePlan {
   size_t ws_bytes;
 };
 
-bool plan_decode(int batch, int max_seqlen, int num_q_heads, int num_kv_heads, int num_splits, DecodePlan* pl) {
-  if (batch < 0 || max_seqlen < 0 || num_kv_heads <= 0 || num_q_heads <= 0) return false;
+bool plan_decode(int batch, int q_len, int max_seqlen, int num_q_heads, int num_kv_heads, int num_splits,
+                 DecodePlan* pl) {
+  if (batch < 0 || q_len <= 0 || max_seqlen < 0 || num_kv_heads <= 0 || num_q_heads <= 0) return false;
   if (num_splits < 0 || num_splits > kMaxSplits) return false;
   const long long max_pages = ((long long)max_seqlen + kPageSize - 1) / kPageSize;
   int split_pages = kMaxSplitPages;
@@ -155,12 +157,19 @@ bool plan_decode(int batch, int max_seqlen, int num_q_heads, int num_kv_heads, i
   if (pl->direct) {
     pl->ws_bytes = 0;
   } else {
-    const size_t slots = (size_t)batch * num_q_heads * max_splits;
+    const size_t slots = (size_t)batch * q_len * num_q_heads * max_splits;
     const size_t o_bytes = (slots * kHeadDim * 4 + 255) / 256 * 256;
     pl->ws_bytes = o_bytes + slots * 2 * 4;
   }
   return true;
 }
+
+// Shared body of sink_attn_decode (q_len = 1) and sink_attn_decode_multi.
+int decode_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                int page_table_stride, const int32_t* seqlens, int batch, int q_len, int max_seqlen, int num_pages,
+                const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale,
+                int num_splits, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                void* stream);
 
 }  // namespace
 }  // namespace sa
@@ -203,15 +212,21 @@ int sink_attn_get_device_error(void* stream) {
 int sink_attn_decode_max_splits(int batch, int max_seqlen, int num_kv_heads, int page_size, int num_splits) {
   if (page_size != kPageSize) return 0;
   DecodePlan pl;
-  if (!plan_decode(batch, max_seqlen, num_kv_heads, num_kv_heads, num_splits, &pl)) return 0;
+  if (!plan_decode(batch, 1, max_seqlen, num_kv_heads, num_kv_heads, num_splits, &pl)) return 0;
   return pl.max_splits;
 }
 
 size_t sink_attn_decode_workspace_bytes(int batch, int max_seqlen, int num_q_heads, int num_kv_heads,
                                         int head_dim, int page_size, int num_splits) {
+  return sink_attn_decode_multi_workspace_bytes(batch, 1, max_seqlen, num_q_heads, num_kv_heads, head_dim,
+                                                page_size, num_splits);
+}
+
+size_t sink_attn_decode_multi_workspace_bytes(int batch, int q_len, int max_seqlen, int num_q_heads,
+                                              int num_kv_heads, int head_dim, int page_size, int num_splits) {
   if (head_dim != kHeadDim || page_size != kPageSize) return (size_t)-1;
   DecodePlan pl;
-  if (!plan_decode(batch, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl)) return (size_t)-1;
+  if (!plan_decode(batch, q_len, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl)) return (size_t)-1;
   return pl.ws_bytes;
 }
 
@@ -220,14 +235,41 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
                      const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
                      float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
                      size_t workspace_bytes, void* stream) {
+  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, 1, max_seqlen, num_pages,
+                     sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out, out_dtype, lse,
+                     workspace, workspace_bytes, stream);
+}
+
+int sink_attn_decode_multi(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                           int page_table_stride, const int32_t* seqlens, int batch, int q_len, int max_seqlen,
+                           int num_pages, const float* sinks, int num_q_heads, int num_kv_heads, int head_dim,
+                           int page_size, float scale, int num_splits, void* out, int out_dtype, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, q_len, max_seqlen,
+                     num_pages, sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out,
+                     out_dtype, lse, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace sa {
+namespace {
+
+int decode_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                int page_table_stride, const int32_t* seqlens, int batch, int q_len, int max_seqlen, int num_pages,
+                const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale,
+                int num_splits, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                void* stream) {
   // ---- validation (nothing is enqueued on failure)
-  if (batch < 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0) return SINK_ATTN_ERR_INVALID_ARG;
+  if (batch < 0 || q_len <= 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+    return SINK_ATTN_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads) return SINK_ATTN_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > kMaxSplits) return SINK_ATTN_ERR_INVALID_ARG;
   if (out_dtype != SINK_ATTN_OUT_BF16 && out_dtype != SINK_ATTN_OUT_F32) return SINK_ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return SINK_ATTN_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || page_size != kPageSize) return SINK_ATTN_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > kMaxGroupDecode) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)(num_q_heads / num_kv_heads) * q_len > kMaxDecodeRows) return SINK_ATTN_ERR_UNSUPPORTED;
   if (batch == 0) return SINK_ATTN_OK;
   if (!q || !k_pages || !v_pages || !page_table || !seqlens || !sinks || !out) return SINK_ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(page_table) ||
@@ -236,9 +278,11 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
   if (num_pages <= 0 || page_table_stride <= 0) return SINK_ATTN_ERR_INVALID_ARG;
   if ((long long)page_table_stride * kPageSize < max_seqlen) return SINK_ATTN_ERR_INVALID_ARG;
   if (batch > 65535 || num_kv_heads > 65535) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)batch * q_len * num_q_heads >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
   if ((long long)num_pages * num_kv_heads * kPageSize >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
   DecodePlan pl;
-  if (!plan_decode(batch, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl)) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!plan_decode(batch, q_len, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl))
+    return SINK_ATTN_ERR_INVALID_ARG;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SINK_ATTN_ERR_INVALID_ARG;
   if (workspace && workspace_bytes < pl.ws_bytes) return SINK_ATTN_ERR_INVALID_ARG;
 
@@ -277,7 +321,7 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
   p.out = out;
   p.lse = lse;
   if (pl.ws_bytes) {
-    const size_t slots = (size_t)batch * num_q_heads * pl.max_splits;
+    const size_t slots = (size_t)batch * q_len * num_q_heads * pl.max_splits;
     p.ws_o = static_cast<float*>(ws);
     p.ws_md = reinterpret_cast<float*>(static_cast<char*>(ws) + (slots * kHeadDim * 4 + 255) / 256 * 256);
   }
@@ -287,6 +331,7 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
   p.hkv = num_kv_heads;
   p.group = num_q_heads / num_kv_heads;
   p.stride = page_table_stride;
+  p.q_len = q_len;
   p.num_splits = num_splits;
   p.split_pages = pl.split_pages;
   p.max_splits = pl.max_splits;
@@ -299,6 +344,11 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
   if (owned) cudaFreeAsync(ws, s);
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }
+
+}  // namespace
+}  // namespace sa
+
+extern "C" {
 
 int sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks, const int32_t* cu_seqlens,
                       int batch, int total_tokens, int max_seqlen, int num_q_heads, int num_kv_heads,

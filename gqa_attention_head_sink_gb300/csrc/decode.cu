@@ -7,20 +7,27 @@
 // d = 1).  A second kernel combines the chunks' (m, d, acc) triples.
 //
 // Work decomposition: one CTA per (chunk, kv head, sequence).  The CTA holds
-// the G = Hq/Hkv query heads that share the kv head, so every page of K/V is
-// read from HBM exactly once.  Roles:
+// every query row that reads the kv head -- the G = Hq/Hkv query heads of the
+// group times the n new tokens of the sequence (n = 1 for plain decode; n > 1
+// for multi-token decode, where new token t sits at position L - n + t and
+// sees keys 0..L - n + t) -- so every page of K/V is read from HBM exactly
+// once.  Row rho = t*G + (h mod G); rows come in tiles of 16 (R = 1, 2 or 4
+// tiles, a template parameter).  Roles:
 //   * warp 4 (producer): reads the page-table entries of the chunk and streams
 //     each (page, kv head) slab -- 16 tokens x 64 dims x bf16 = 2 KiB of K and
 //     2 KiB of V, contiguous in the [page, kv_head, slot, dim] layout -- into a
 //     ring of shared-memory stages with 2-D TMA copies (128-byte swizzle), one
 //     mbarrier per stage completing on the transferred bytes;
-//   * warps 0..3 (consumers): warp w takes pages w, w+4, ...  For one page it
-//     computes S = Q K^T (16 rows = query heads of the group, padded; 16
-//     tokens) and O += P V with warp-level bf16 MMAs (m16n8k16, fp32
-//     accumulate), the online softmax in registers, and releases the stage as
-//     soon as K and V are in registers.
-// The four warps' states are merged in shared memory; with a single chunk
-// the CTA writes the normalised output directly, otherwise its partial state.
+//   * warps 0..3 (consumers): warp w owns row tile w % R and takes pages
+//     w / R, w / R + 4 / R, ...  For one page it computes S = Q K^T (16 rows,
+//     padded; 16 tokens) and O += P V with warp-level bf16 MMAs (m16n8k16,
+//     fp32 accumulate), the online softmax in registers, and releases the
+//     stage (each stage is released by the R warps that read it) as soon as
+//     K and V are in registers.
+// The states of the warps sharing a row tile are merged in shared memory;
+// with a single chunk the CTA writes the normalised output directly,
+// otherwise its partial state.  Work is HBM-bound for up to 64 rows (at most
+// 64 flop per byte of K/V), so the warp-level MMAs keep up with the copies.
 //
 // Fragment layouts (m16n8k16): lane = 4*r + qd.  The head dimension is used in
 // a permuted order that is the same for Q and K (a dot product does not care),
@@ -44,7 +51,7 @@ constexpr int kStages = 8;
 constexpr int kSlabBytes = kPage * kD * 2;      // 2048
 constexpr int kStageBytes = 2 * kSlabBytes;     // K + V
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kRows = 16;                       // MMA rows = query heads per group (padded)
+constexpr int kRows = 16;                       // MMA rows of one row tile
 // merge scratch per warp: m[16], d[16], o[16][64]
 constexpr int kScratchFloatsPerWarp = kRows * 2 + kRows * kD;
 static_assert(kConsumerWarps * kScratchFloatsPerWarp * 4 <= kRingBytes, "merge scratch aliases the ring");
@@ -60,10 +67,13 @@ __device__ __forceinline__ void chunk_range(const DecodeParams& p, int L, int s,
 }  // namespace
 
 // Four CTAs per SM (96 registers a thread) keep enough page copies in flight
-// to approach the HBM bandwidth.
+// to approach the HBM bandwidth.  R = row tiles of 16 rows (1, 2 or 4).
+template <int R>
 __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 const DecodeParams p) {
+  static_assert(R == 1 || R == 2 || R == 4, "row tiles per CTA");
+  constexpr int kPhases = kConsumerWarps / R;  // warps that share one row tile, each taking every kPhases-th page
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   // a length beyond the page-table row is clamped: never read past the row
   const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
@@ -82,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], R);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -126,22 +136,31 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
 
   // -------------------------------------------------------------- consumers
   const int r = lane >> 2, qd = lane & 3;
-  const int G = p.group;
-  const int h_r = g * G + r, h_r8 = g * G + r + 8;
-  const bool row_ok = r < G, row8_ok = r + 8 < G;
+  const int rt = warp % R, ph = warp / R;  // row tile, page phase
+  const int G = p.group, nrows = G * p.q_len;
+  const int rho = rt * kRows + r, rho8 = rho + 8;
+  const bool row_ok = rho < nrows, row8_ok = rho8 < nrows;
+  // new token t and query head h of rows rho and rho + 8
+  const int t_r = rho / G, t_r8 = rho8 / G;
+  const int h_r = g * G + rho - t_r * G, h_r8 = g * G + rho8 - t_r8 * G;
+  // keys visible to a row: positions < lim (causal among the new tokens);
+  // padding rows take every valid key so that their (unused) state stays finite
+  const int lim_r = row_ok ? L - p.q_len + t_r + 1 : L;
+  const int lim_r8 = row8_ok ? L - p.q_len + t_r8 + 1 : L;
 
-  // Query fragments: row r holds dims [16qd, 16qd+16) of head h_r.
+  // Query fragments: row r holds dims [16qd, 16qd+16) of its head.
   uint32_t qa[4][4];
   {
     uint4 lo_r = make_uint4(0, 0, 0, 0), hi_r = lo_r, lo_r8 = lo_r, hi_r8 = lo_r;
-    const uint4* qb = reinterpret_cast<const uint4*>(p.q + (size_t)b * p.hq * kD);
     if (row_ok) {
-      lo_r = __ldg(qb + (h_r * kD + 16 * qd) / 8);
-      hi_r = __ldg(qb + (h_r * kD + 16 * qd) / 8 + 1);
+      const uint4* qr = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.q_len + t_r) * p.hq + h_r) * kD);
+      lo_r = __ldg(qr + 2 * qd);
+      hi_r = __ldg(qr + 2 * qd + 1);
     }
     if (row8_ok) {
-      lo_r8 = __ldg(qb + (h_r8 * kD + 16 * qd) / 8);
-      hi_r8 = __ldg(qb + (h_r8 * kD + 16 * qd) / 8 + 1);
+      const uint4* qr = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.q_len + t_r8) * p.hq + h_r8) * kD);
+      lo_r8 = __ldg(qr + 2 * qd);
+      hi_r8 = __ldg(qr + 2 * qd + 1);
     }
     const uint32_t wr[8] = {lo_r.x, lo_r.y, lo_r.z, lo_r.w, hi_r.x, hi_r.y, hi_r.z, hi_r.w};
     const uint32_t wr8[8] = {lo_r8.x, lo_r8.y, lo_r8.z, lo_r8.w, hi_r8.x, hi_r8.y, hi_r8.z, hi_r8.w};
@@ -155,9 +174,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   }
 
   // Online-softmax state for rows r and r+8 (log2 domain).  Only the first
-  // chunk's first warp starts from the sink: m = sink * log2(e), d = 1.
+  // chunk's first warp of each row tile starts from the sink: m = sink *
+  // log2(e), d = 1.
   float m_r = -INFINITY, m_r8 = -INFINITY, d_r = 0.f, d_r8 = 0.f;
-  if (s == 0 && warp == 0) {
+  if (s == 0 && ph == 0) {
     m_r = row_ok ? __ldg(p.sinks + h_r) * kLog2e : -INFINITY;
     m_r8 = row8_ok ? __ldg(p.sinks + h_r8) * kLog2e : -INFINITY;
     if (qd == 0) {
@@ -170,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
   const float sl2 = p.scale_log2;
-  for (int i = warp; i < count; i += kConsumerWarps) {
+  for (int i = ph; i < count; i += kPhases) {
     const int st = i % kStages;
     if (!mbar_wait(&full[st], (i / kStages) & 1, p.err, kErrDecodeFull, p.wait_limit_ns)) {
       *abort_flag = 1;
@@ -193,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
 
-    const int valid = min(kPage, L - (pg0 + i) * kPage);  // >= 1
+    const int base = (pg0 + i) * kPage;
+    const int valid = min(kPage, L - base);  // >= 1
     if (valid < kPage) {  // tail page: unused slots may hold anything (even NaN)
       const uint4 z = make_uint4(0, 0, 0, 0);
       if (t0 >= valid) va = z;
@@ -213,13 +234,15 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
       mma_16816_bf16(sc[nt], qa[2], kb.x, kb.y);
       mma_16816_bf16(sc[nt], qa[3], kb.z, kb.w);
     }
-    // scale to log2 units, mask slots past the sequence end
+    // scale to log2 units, mask slots past each row's last visible key
+    // (lim <= L, so slots past the sequence end are always masked)
+    const int vis_r = lim_r - base, vis_r8 = lim_r8 - base;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = nt * 8 + 2 * qd + (e & 1);
-        sc[nt][e] = tok < valid ? sc[nt][e] * sl2 : -INFINITY;
+        sc[nt][e] = tok < (e < 2 ? vis_r : vis_r8) ? sc[nt][e] * sl2 : -INFINITY;
       }
     }
     float mx_r = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
@@ -228,17 +251,20 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
     mx_r = fmaxf(mx_r, __shfl_xor_sync(0xffffffffu, mx_r, 2));
     mx_r8 = fmaxf(mx_r8, __shfl_xor_sync(0xffffffffu, mx_r8, 1));
     mx_r8 = fmaxf(mx_r8, __shfl_xor_sync(0xffffffffu, mx_r8, 2));
-    const float mn_r = fmaxf(m_r, mx_r), mn_r8 = fmaxf(m_r8, mx_r8);  // finite: the page has a valid slot
-    const float al_r = fast_exp2(m_r - mn_r), al_r8 = fast_exp2(m_r8 - mn_r8);
+    const float mn_r = fmaxf(m_r, mx_r), mn_r8 = fmaxf(m_r8, mx_r8);
+    // -inf only while a row has seen neither the sink nor a key: subtract 0
+    // then, so that alpha and every weight come out 0 instead of NaN
+    const float ms_r = mn_r == -INFINITY ? 0.f : mn_r, ms_r8 = mn_r8 == -INFINITY ? 0.f : mn_r8;
+    const float al_r = fast_exp2(m_r - ms_r), al_r8 = fast_exp2(m_r8 - ms_r8);
     m_r = mn_r;
     m_r8 = mn_r8;
     float pr[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      pr[nt][0] = fast_exp2(sc[nt][0] - mn_r);
-      pr[nt][1] = fast_exp2(sc[nt][1] - mn_r);
-      pr[nt][2] = fast_exp2(sc[nt][2] - mn_r8);
-      pr[nt][3] = fast_exp2(sc[nt][3] - mn_r8);
+      pr[nt][0] = fast_exp2(sc[nt][0] - ms_r);
+      pr[nt][1] = fast_exp2(sc[nt][1] - ms_r);
+      pr[nt][2] = fast_exp2(sc[nt][2] - ms_r8);
+      pr[nt][3] = fast_exp2(sc[nt][3] - ms_r8);
     }
     uint32_t pa[4];
     pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
@@ -264,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
     }
   }
 
-  // ---------------------------------------------- merge the four warps' states
+  // ------------------------- merge the states of the warps sharing a row tile
   d_r += __shfl_xor_sync(0xffffffffu, d_r, 1);
   d_r += __shfl_xor_sync(0xffffffffu, d_r, 2);
   d_r8 += __shfl_xor_sync(0xffffffffu, d_r8, 1);
@@ -290,68 +316,72 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   named_barrier(1, kConsumerWarps * 32);
 
   const int tid = threadIdx.x;  // 0..127
-  const int row = tid >> 3, c8 = (tid & 7) * 8;
-  if (row >= G) return;
-  const float* base = reinterpret_cast<const float*>(smem);
-  float M = -INFINITY;
+  const int c8 = (tid & 7) * 8;
+  const float* scratch = reinterpret_cast<const float*>(smem);
+  for (int row = tid >> 3; row < nrows; row += 16) {
+    const int rr = row % kRows, rt_row = row / kRows;
+    float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, base[w * kScratchFloatsPerWarp + row]);
-  float W = 0.f, acc[8];
+    for (int k = 0; k < kPhases; ++k) M = fmaxf(M, scratch[(rt_row + R * k) * kScratchFloatsPerWarp + rr]);
+    float W = 0.f, acc[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  if (M != -INFINITY) {
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    if (M != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float* ws = base + w * kScratchFloatsPerWarp;
-      const float mw = ws[row];
-      if (mw == -INFINITY) continue;
-      const float f = fast_exp2(mw - M);
-      W += ws[kRows + row] * f;
-      const float* ow = ws + 2 * kRows + row * kD + c8;
+      for (int k = 0; k < kPhases; ++k) {
+        const float* ws = scratch + (rt_row + R * k) * kScratchFloatsPerWarp;
+        const float mw = ws[rr];
+        if (mw == -INFINITY) continue;
+        const float f = fast_exp2(mw - M);
+        W += ws[kRows + rr] * f;
+        const float* ow = ws + 2 * kRows + rr * kD + c8;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += ow[e] * f;
+        for (int e = 0; e < 8; ++e) acc[e] += ow[e] * f;
+      }
     }
-  }
-  const int h = g * G + row;
-  if (p.direct) {
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    const size_t o_off = ((size_t)b * p.hq + h) * kD + c8;
-    if (p.out_f32) {
-      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o_off);
-      dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-      dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+    const int t = row / G;
+    const size_t qrow = ((size_t)b * p.q_len + t) * p.hq + g * G + (row - t * G);  // (sequence, token, head)
+    if (p.direct) {
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      const size_t o_off = qrow * kD + c8;
+      if (p.out_f32) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o_off);
+        dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+      } else {
+        uint4 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = v;
+      }
+      if (p.lse && c8 == 0) p.lse[qrow] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
     } else {
-      uint4 v;
-      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-      v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = v;
-    }
-    if (p.lse && c8 == 0) p.lse[(size_t)b * p.hq + h] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
-  } else {
-    const size_t slot = ((size_t)b * p.hq + h) * p.max_splits + s;
-    float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kD + c8);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    if (c8 == 0) {
-      p.ws_md[slot * 2] = M;
-      p.ws_md[slot * 2 + 1] = W;
+      const size_t slot = qrow * p.max_splits + s;
+      float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kD + c8);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      if (c8 == 0) {
+        p.ws_md[slot * 2] = M;
+        p.ws_md[slot * 2 + 1] = W;
+      }
     }
   }
 }
 
-// Combine the chunks' partial states: one warp per (sequence, query head).
-// Lane l owns output dims 2l, 2l+1.  Chunk c contributes with weight
-// 2^(m_c - M), M = max_c m_c; chunks that saw nothing have m_c = -inf.
+// Combine the chunks' partial states: one warp per (sequence, new token,
+// query head) row.  Lane l owns output dims 2l, 2l+1.  Chunk c contributes
+// with weight 2^(m_c - M), M = max_c m_c; chunks that saw nothing have
+// m_c = -inf.
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  const int b = wid / p.hq, h = wid % p.hq;
+  const int b = wid / (p.hq * p.q_len);
   if (b >= p.batch) return;
   const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
   int n, pg0, pg1;
   chunk_range(p, L, 0, n, pg0, pg1);
-  const size_t slot0 = ((size_t)b * p.hq + h) * p.max_splits;
+  const size_t slot0 = (size_t)wid * p.max_splits;
   const float* md = p.ws_md + slot0 * 2;
   float M = -INFINITY;
   for (int c = lane; c < n; c += 32) M = fmaxf(M, md[2 * c]);
@@ -370,23 +400,31 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     }
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
-  const size_t o_off = ((size_t)b * p.hq + h) * kD + 2 * lane;
+  const size_t o_off = (size_t)wid * kD + 2 * lane;
   if (p.out_f32) {
     *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.out) + o_off) = make_float2(a0 * inv, a1 * inv);
   } else {
     *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = pack_bf16x2(a0 * inv, a1 * inv);
   }
-  if (p.lse && lane == 0) p.lse[(size_t)b * p.hq + h] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+  if (p.lse && lane == 0) p.lse[wid] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
 }
 
 size_t decode_smem_bytes() { return kRingBytes + 2 * kStages * 8 + 16 + 1024; }
 
-cudaError_t decode_configure() {
+template <int R>
+static cudaError_t configure_one() {
   // Prefer shared memory over L1 so four CTAs' rings fit on an SM.
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<R>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(decode_split_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)decode_smem_bytes());
+}
+
+cudaError_t decode_configure() {
+  cudaError_t e = configure_one<1>();
+  if (e == cudaSuccess) e = configure_one<2>();
+  if (e == cudaSuccess) e = configure_one<4>();
+  return e;
 }
 int decode_threads() { return kThreads; }
 
@@ -397,10 +435,16 @@ namespace sa {
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                           cudaStream_t stream) {
   dim3 grid(p.max_splits, p.hkv, p.batch);
-  decode_split_kernel<<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
+  const int rows = p.group * p.q_len;
+  if (rows <= 16)
+    decode_split_kernel<1><<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
+  else if (rows <= 32)
+    decode_split_kernel<2><<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
+  else
+    decode_split_kernel<4><<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.direct) return e;
-  const long long warps = (long long)p.batch * p.hq;
+  const long long warps = (long long)p.batch * p.q_len * p.hq;
   decode_merge_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -10,16 +10,17 @@
 namespace sa {
 
 struct DecodeParams {
-  const __nv_bfloat16* q;     // [B, Hq, 64]
+  const __nv_bfloat16* q;     // [B, q_len, Hq, 64]
   const int32_t* page_table;  // [B, stride]
   const int32_t* seqlens;     // [B]
   const float* sinks;         // [Hq]
-  void* out;                  // [B, Hq, 64] bf16 or fp32
-  float* lse;                 // [B, Hq] or null
-  float* ws_o;                // [B, Hq, max_splits, 64] partial weighted sums
-  float* ws_md;               // [B, Hq, max_splits, 2] partial (m, d), m in log2 units
+  void* out;                  // [B, q_len, Hq, 64] bf16 or fp32
+  float* lse;                 // [B, q_len, Hq] or null
+  float* ws_o;                // [B, q_len, Hq, max_splits, 64] partial weighted sums
+  float* ws_md;               // [B, q_len, Hq, max_splits, 2] partial (m, d), m in log2 units
   unsigned* err;              // device error word
   int batch, hq, hkv, group, stride;
+  int q_len;        // new query tokens per sequence (the last q_len of its cache); group * q_len <= 64
   int num_splits;   // > 0: requested chunks per sequence; 0: by length
   int split_pages;  // pages per chunk when num_splits == 0
   int max_splits;   // grid extent of the chunk dimension
@@ -42,6 +43,7 @@ __host__ __device__ inline int decode_num_chunks(int npages, int num_splits, int
   return (npages + chunk - 1) / chunk;
 }
 
+template <int R>
 __global__ void decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                                     const DecodeParams p);
 __global__ void decode_merge_kernel(const DecodeParams p);

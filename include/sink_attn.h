@@ -139,6 +139,47 @@ size_t sink_attn_decode_workspace_bytes(int batch, int max_seqlen, int num_q_hea
                                         int num_splits);
 
 /*
+ * Multi-token decode: q_len new query tokens per sequence against the paged
+ * KV cache, for speculative or multi-token-prediction drafts that verify
+ * several tokens in one step ("GPT-OSS on day 0" mentions both; the
+ * attention is the one of section Sink Attention, split along the key
+ * length exactly as in sink_attn_decode, sink only in the first chunk).
+ *
+ * The q_len new tokens are the LAST q_len tokens already written to each
+ * sequence's cache: with L = seqlens[b], new token t (0-based) sits at
+ * position L - q_len + t and sees keys 0 .. L - q_len + t (causal among the
+ * new tokens, every older token visible).  If L < q_len, the tokens placed
+ * before the cache start see no key: out = 0 and lse = sink (or -inf).
+ *
+ *   q       bf16 [batch, q_len, num_q_heads, head_dim]
+ *   out     [batch, q_len, num_q_heads, head_dim], bf16 or fp32 per out_dtype
+ *   lse     optional fp32 [batch, q_len, num_q_heads]; NULL to skip
+ *   q_len   >= 1, with (num_q_heads / num_kv_heads) * q_len <= 64 (the query
+ *           rows that share one kv head are processed together, so every
+ *           page is read once for all of them); e.g. q_len <= 8 at group 8.
+ *   workspace
+ *           at least sink_attn_decode_multi_workspace_bytes(...) bytes,
+ *           256-byte aligned, or NULL (allocated in stream order).
+ * Every other argument, limit and error is that of sink_attn_decode, which
+ * equals this call with q_len = 1.
+ */
+int sink_attn_decode_multi(const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* page_table, int page_table_stride,
+                           const int32_t* seqlens, int batch, int q_len, int max_seqlen,
+                           int num_pages, const float* sinks, int num_q_heads, int num_kv_heads,
+                           int head_dim, int page_size, float scale, int num_splits,
+                           void* out, int out_dtype, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace sink_attn_decode_multi needs (0 when no sequence is
+ * split); (size_t)-1 for arguments it would reject on size grounds.
+ */
+size_t sink_attn_decode_multi_workspace_bytes(int batch, int q_len, int max_seqlen, int num_q_heads,
+                                              int num_kv_heads, int head_dim, int page_size,
+                                              int num_splits);
+
+/*
  * The largest number of chunks any sequence gets for these arguments
  * (the grid's chunk dimension); 0 for arguments sink_attn_decode would reject.
  */

@@ -139,3 +139,43 @@ def test_decode_planning(lib):
     assert n == slots * 64 * 4 + slots * 2 * 4
     with pytest.raises(sa.SinkAttnError):
         sa.sink_attn_decode_workspace_bytes(1, 16, 64, 8, 128, 16, 0)
+
+
+def _decode_multi_call(lib, q_len, **kw):
+    args = dict(q=8 * 16, k=8 * 32, v=8 * 48, table=8 * 64, stride=4, seqlens=8 * 80, batch=2, max_seqlen=64,
+                num_pages=8, sinks=8 * 96, hq=64, hkv=8, d=64, page=16, scale=0.125, splits=0, out=8 * 112,
+                out_dtype=1)
+    args.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731  (fake, never dereferenced)
+    return lib.sink_attn_decode_multi(P(args["q"]), P(args["k"]), P(args["v"]), P(args["table"]), args["stride"],
+                                      P(args["seqlens"]), args["batch"], q_len, args["max_seqlen"],
+                                      args["num_pages"], P(args["sinks"]), args["hq"], args["hkv"], args["d"],
+                                      args["page"], args["scale"], args["splits"], P(args["out"]),
+                                      args["out_dtype"], None, None, 0, None)
+
+
+@pytest.mark.parametrize("q_len,kw,status", [
+    (0, {}, 1),                       # at least one new token
+    (-3, {}, 1),
+    (9, {}, 2),                       # 8 heads x 9 tokens = 72 rows share a kv head: more than 64
+    (5, dict(hq=64, hkv=4), 2),       # 16 x 5 = 80 rows
+    (4, dict(hq=64, hkv=2), 2),       # group of 32: beyond one row block per head group
+    (2, dict(d=128), 2),
+    (2, dict(q=8 * 16 + 8), 1),       # misaligned
+])
+def test_decode_multi_rejects_bad_arguments_on_host(lib, q_len, kw, status):
+    assert _decode_multi_call(lib, q_len, **kw) == status
+
+
+def test_decode_multi_empty_batch_is_noop(lib):
+    assert _decode_multi_call(lib, 8, batch=0, q=None, out=None) == 0
+
+
+def test_decode_multi_workspace(lib):
+    # q_len rows per (sequence, head): q_len times the single-token workspace
+    one = sa.sink_attn_decode_workspace_bytes(64, 8192, 64, 8, 64, 16, 8)
+    assert sa.sink_attn_decode_multi_workspace_bytes(64, 1, 8192, 64, 8, 64, 16, 8) == one
+    slots = 64 * 4 * 64 * 8
+    assert sa.sink_attn_decode_multi_workspace_bytes(64, 4, 8192, 64, 8, 64, 16, 8) == slots * 64 * 4 + slots * 8
+    with pytest.raises(sa.SinkAttnError):
+        sa.sink_attn_decode_multi_workspace_bytes(64, 0, 8192, 64, 8, 64, 16, 8)
