@@ -27,7 +27,10 @@ constexpr int kHeadDim = 64;
 constexpr int kPageSize = 16;
 constexpr int kMaxSplits = 256;
 constexpr int kMaxGroupDecode = 16;
-constexpr int kMaxDecodeRows = 64;  // query rows per kv head in decode: group * new tokens
+// Query rows per kv head (group * new tokens) above which decode runs on the
+// tensor cores (128-row tiles) instead of warp-level MMAs (16-row tiles).
+constexpr int kTensorCoreMinRows = 17;
+constexpr int kMaxDecodeTokens = 4096;  // new tokens per sequence in one decode call
 constexpr int kMaxDevices = 64;
 // Chunk sizing for num_splits == 0: aim for about this many CTAs in the
 // chunk grid (8 per SM of a 152-SM GB300) with 16..128 pages per chunk.
@@ -113,14 +116,16 @@ int encode_rows64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t ro
 }
 
 // 3-D bf16 tensor map over a packed [tokens, heads, 64] tensor, boxes of
-// box_tokens tokens x 1 head x 64 dims (one tile of one head), 128-byte swizzle.
-int encode_tokens_heads(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads, uint32_t box_tokens) {
+// box_tokens tokens x box_heads heads x 64 dims, 128-byte swizzle.  A box
+// lands as box_tokens * box_heads rows of 128 bytes, token-major.
+int encode_tokens_heads(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads, uint32_t box_tokens,
+                        uint32_t box_heads = 1) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   int st = get_encoder(&enc);
   if (st) return st;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
-  cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, box_tokens};
+  cuuint32_t box[3] = {(cuuint32_t)kHeadDim, box_heads, box_tokens};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -135,9 +140,20 @@ struct DecodePlan {
   size_t ws_bytes;
 };
 
+// Rows of one tensor-core decode tile are (new token, query head) pairs of one
+// kv head: this many tokens per tile, and this many tiles per sequence.
+int decode_tokens_per_tile(int group, int q_len) { return std::max(1, std::min(q_len, kDecodeTcRows / group)); }
+int decode_row_tiles(int group, int q_len) {
+  if (group * q_len < kTensorCoreMinRows) return 1;
+  const int tpt = decode_tokens_per_tile(group, q_len);
+  return (q_len + tpt - 1) / tpt;
+}
+
 bool plan_decode(int batch, int q_len, int max_seqlen, int num_q_heads, int num_kv_heads, int num_splits,
                  DecodePlan* pl) {
   if (batch < 0 || q_len <= 0 || max_seqlen < 0 || num_kv_heads <= 0 || num_q_heads <= 0) return false;
+  if (num_q_heads % num_kv_heads) return false;
+  const int row_tiles = decode_row_tiles(num_q_heads / num_kv_heads, q_len);
   if (num_splits < 0 || num_splits > kMaxSplits) return false;
   const long long max_pages = ((long long)max_seqlen + kPageSize - 1) / kPageSize;
   int split_pages = kMaxSplitPages;
@@ -145,7 +161,8 @@ bool plan_decode(int batch, int q_len, int max_seqlen, int num_q_heads, int num_
   if (num_splits > 0) {
     max_splits = (int)std::max(1LL, std::min<long long>(num_splits, max_pages));
   } else {
-    long long sp = ((long long)batch * num_kv_heads * max_pages + kDecodeTargetCtas - 1) / kDecodeTargetCtas;
+    long long sp = ((long long)batch * row_tiles * num_kv_heads * max_pages + kDecodeTargetCtas - 1) /
+                   kDecodeTargetCtas;
     sp = std::min<long long>(kMaxSplitPages, std::max<long long>(kMinSplitPages, sp));
     if ((max_pages + sp - 1) / sp > kMaxSplits) sp = (max_pages + kMaxSplits - 1) / kMaxSplits;
     split_pages = (int)sp;
@@ -269,7 +286,10 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   if (!(scale > 0.f) || !std::isfinite(scale)) return SINK_ATTN_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || page_size != kPageSize) return SINK_ATTN_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > kMaxGroupDecode) return SINK_ATTN_ERR_UNSUPPORTED;
-  if ((long long)(num_q_heads / num_kv_heads) * q_len > kMaxDecodeRows) return SINK_ATTN_ERR_UNSUPPORTED;
+  if (q_len > kMaxDecodeTokens) return SINK_ATTN_ERR_UNSUPPORTED;
+  const int group = num_q_heads / num_kv_heads;
+  const bool tensor_cores = group * q_len >= kTensorCoreMinRows;
+  const int row_tiles = decode_row_tiles(group, q_len);
   if (batch == 0) return SINK_ATTN_OK;
   if (!q || !k_pages || !v_pages || !page_table || !seqlens || !sinks || !out) return SINK_ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(page_table) ||
@@ -277,7 +297,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
     return SINK_ATTN_ERR_INVALID_ARG;
   if (num_pages <= 0 || page_table_stride <= 0) return SINK_ATTN_ERR_INVALID_ARG;
   if ((long long)page_table_stride * kPageSize < max_seqlen) return SINK_ATTN_ERR_INVALID_ARG;
-  if (batch > 65535 || num_kv_heads > 65535) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)batch * row_tiles > 65535 || num_kv_heads > 65535) return SINK_ATTN_ERR_UNSUPPORTED;
   if ((long long)batch * q_len * num_q_heads >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
   if ((long long)num_pages * num_kv_heads * kPageSize >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
   DecodePlan pl;
@@ -294,7 +314,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_decode_attr_set[dev]) {
-      if (decode_configure() != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+      if (decode_configure() != cudaSuccess || decode_tc_configure() != cudaSuccess) return SINK_ATTN_ERR_CUDA;
       g_decode_attr_set[dev] = true;
     }
   }
@@ -302,6 +322,11 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   CUtensorMap kmap, vmap;
   if ((st = encode_rows64(&kmap, k_pages, rows, kHeadDim * 2, kPageSize))) return st;
   if ((st = encode_rows64(&vmap, v_pages, rows, kHeadDim * 2, kPageSize))) return st;
+  const int tokens_per_tile = decode_tokens_per_tile(group, q_len);
+  CUtensorMap qmap;  // tensor-core path: q as [batch * q_len tokens, Hq, 64], one box = one row tile
+  if (tensor_cores &&
+      (st = encode_tokens_heads(&qmap, q, (uint64_t)batch * q_len, num_q_heads, tokens_per_tile, group)))
+    return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = workspace;
@@ -332,6 +357,8 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   p.group = num_q_heads / num_kv_heads;
   p.stride = page_table_stride;
   p.q_len = q_len;
+  p.tokens_per_tile = tokens_per_tile;
+  p.row_tiles = row_tiles;
   p.num_splits = num_splits;
   p.split_pages = pl.split_pages;
   p.max_splits = pl.max_splits;
@@ -340,7 +367,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.withhold_copies = withhold_copies();
-  cudaError_t e = launch_decode(kmap, vmap, p, s);
+  const cudaError_t e = tensor_cores ? launch_decode_tc(qmap, kmap, vmap, p, s) : launch_decode(kmap, vmap, p, s);
   if (owned) cudaFreeAsync(ws, s);
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }

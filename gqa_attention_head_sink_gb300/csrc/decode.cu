@@ -11,23 +11,21 @@
 // group times the n new tokens of the sequence (n = 1 for plain decode; n > 1
 // for multi-token decode, where new token t sits at position L - n + t and
 // sees keys 0..L - n + t) -- so every page of K/V is read from HBM exactly
-// once.  Row rho = t*G + (h mod G); rows come in tiles of 16 (R = 1, 2 or 4
-// tiles, a template parameter).  Roles:
+// once.  Row rho = t*G + (h mod G), at most 16 rows (one MMA row tile; more
+// rows go to the tensor-core kernel of decode_tc.cu).  Roles:
 //   * warp 4 (producer): reads the page-table entries of the chunk and streams
 //     each (page, kv head) slab -- 16 tokens x 64 dims x bf16 = 2 KiB of K and
 //     2 KiB of V, contiguous in the [page, kv_head, slot, dim] layout -- into a
 //     ring of shared-memory stages with 2-D TMA copies (128-byte swizzle), one
 //     mbarrier per stage completing on the transferred bytes;
-//   * warps 0..3 (consumers): warp w owns row tile w % R and takes pages
-//     w / R, w / R + 4 / R, ...  For one page it computes S = Q K^T (16 rows,
-//     padded; 16 tokens) and O += P V with warp-level bf16 MMAs (m16n8k16,
-//     fp32 accumulate), the online softmax in registers, and releases the
-//     stage (each stage is released by the R warps that read it) as soon as
-//     K and V are in registers.
-// The states of the warps sharing a row tile are merged in shared memory;
-// with a single chunk the CTA writes the normalised output directly,
-// otherwise its partial state.  Work is HBM-bound for up to 64 rows (at most
-// 64 flop per byte of K/V), so the warp-level MMAs keep up with the copies.
+//   * warps 0..3 (consumers): warp w takes pages w, w+4, ...  For one page it
+//     computes S = Q K^T (16 rows, padded; 16 tokens) and O += P V with
+//     warp-level bf16 MMAs (m16n8k16, fp32 accumulate), the online softmax in
+//     registers, and releases the stage as soon as K and V are in registers.
+// The four warps' states are merged in shared memory; with a single chunk
+// the CTA writes the normalised output directly, otherwise its partial
+// state.  At 16 rows the work is at most 16 flop per byte of K/V, well
+// within what the warp-level MMAs sustain at full HBM bandwidth.
 //
 // Fragment layouts (m16n8k16): lane = 4*r + qd.  The head dimension is used in
 // a permuted order that is the same for Q and K (a dot product does not care),
@@ -67,13 +65,10 @@ __device__ __forceinline__ void chunk_range(const DecodeParams& p, int L, int s,
 }  // namespace
 
 // Four CTAs per SM (96 registers a thread) keep enough page copies in flight
-// to approach the HBM bandwidth.  R = row tiles of 16 rows (1, 2 or 4).
-template <int R>
+// to approach the HBM bandwidth.
 __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 const DecodeParams p) {
-  static_assert(R == 1 || R == 2 || R == 4, "row tiles per CTA");
-  constexpr int kPhases = kConsumerWarps / R;  // warps that share one row tile, each taking every kPhases-th page
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   // a length beyond the page-table row is clamped: never read past the row
   const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
@@ -92,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], R);
+      mbar_init(&empty[i], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -136,9 +131,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
 
   // -------------------------------------------------------------- consumers
   const int r = lane >> 2, qd = lane & 3;
-  const int rt = warp % R, ph = warp / R;  // row tile, page phase
-  const int G = p.group, nrows = G * p.q_len;
-  const int rho = rt * kRows + r, rho8 = rho + 8;
+  const int G = p.group, nrows = G * p.q_len;  // <= 16
+  const int rho = r, rho8 = r + 8;
   const bool row_ok = rho < nrows, row8_ok = rho8 < nrows;
   // new token t and query head h of rows rho and rho + 8
   const int t_r = rho / G, t_r8 = rho8 / G;
@@ -174,10 +168,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   }
 
   // Online-softmax state for rows r and r+8 (log2 domain).  Only the first
-  // chunk's first warp of each row tile starts from the sink: m = sink *
-  // log2(e), d = 1.
+  // chunk's first warp starts from the sink: m = sink * log2(e), d = 1.
   float m_r = -INFINITY, m_r8 = -INFINITY, d_r = 0.f, d_r8 = 0.f;
-  if (s == 0 && ph == 0) {
+  if (s == 0 && warp == 0) {
     m_r = row_ok ? __ldg(p.sinks + h_r) * kLog2e : -INFINITY;
     m_r8 = row8_ok ? __ldg(p.sinks + h_r8) * kLog2e : -INFINITY;
     if (qd == 0) {
@@ -190,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
   const float sl2 = p.scale_log2;
-  for (int i = ph; i < count; i += kPhases) {
+  for (int i = warp; i < count; i += kConsumerWarps) {
     const int st = i % kStages;
     if (!mbar_wait(&full[st], (i / kStages) & 1, p.err, kErrDecodeFull, p.wait_limit_ns)) {
       *abort_flag = 1;
@@ -290,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
     }
   }
 
-  // ------------------------- merge the states of the warps sharing a row tile
+  // ---------------------------------------------- merge the four warps' states
   d_r += __shfl_xor_sync(0xffffffffu, d_r, 1);
   d_r += __shfl_xor_sync(0xffffffffu, d_r, 2);
   d_r8 += __shfl_xor_sync(0xffffffffu, d_r8, 1);
@@ -316,56 +309,54 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   named_barrier(1, kConsumerWarps * 32);
 
   const int tid = threadIdx.x;  // 0..127
-  const int c8 = (tid & 7) * 8;
+  const int row = tid >> 3, c8 = (tid & 7) * 8;
+  if (row >= nrows) return;
   const float* scratch = reinterpret_cast<const float*>(smem);
-  for (int row = tid >> 3; row < nrows; row += 16) {
-    const int rr = row % kRows, rt_row = row / kRows;
-    float M = -INFINITY;
+  float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kPhases; ++k) M = fmaxf(M, scratch[(rt_row + R * k) * kScratchFloatsPerWarp + rr]);
-    float W = 0.f, acc[8];
+  for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scratch[w * kScratchFloatsPerWarp + row]);
+  float W = 0.f, acc[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    if (M != -INFINITY) {
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  if (M != -INFINITY) {
 #pragma unroll
-      for (int k = 0; k < kPhases; ++k) {
-        const float* ws = scratch + (rt_row + R * k) * kScratchFloatsPerWarp;
-        const float mw = ws[rr];
-        if (mw == -INFINITY) continue;
-        const float f = fast_exp2(mw - M);
-        W += ws[kRows + rr] * f;
-        const float* ow = ws + 2 * kRows + rr * kD + c8;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float* ws = scratch + w * kScratchFloatsPerWarp;
+      const float mw = ws[row];
+      if (mw == -INFINITY) continue;
+      const float f = fast_exp2(mw - M);
+      W += ws[kRows + row] * f;
+      const float* ow = ws + 2 * kRows + row * kD + c8;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += ow[e] * f;
-      }
+      for (int e = 0; e < 8; ++e) acc[e] += ow[e] * f;
     }
-    const int t = row / G;
-    const size_t qrow = ((size_t)b * p.q_len + t) * p.hq + g * G + (row - t * G);  // (sequence, token, head)
-    if (p.direct) {
-      const float inv = W > 0.f ? 1.f / W : 0.f;
-      const size_t o_off = qrow * kD + c8;
-      if (p.out_f32) {
-        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o_off);
-        dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-        dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-      } else {
-        uint4 v;
-        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-        v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = v;
-      }
-      if (p.lse && c8 == 0) p.lse[qrow] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+  }
+  const int t = row / G;
+  const size_t qrow = ((size_t)b * p.q_len + t) * p.hq + g * G + (row - t * G);  // (sequence, token, head)
+  if (p.direct) {
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    const size_t o_off = qrow * kD + c8;
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o_off);
+      dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+      dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
     } else {
-      const size_t slot = qrow * p.max_splits + s;
-      float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kD + c8);
-      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-      if (c8 == 0) {
-        p.ws_md[slot * 2] = M;
-        p.ws_md[slot * 2 + 1] = W;
-      }
+      uint4 v;
+      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = v;
+    }
+    if (p.lse && c8 == 0) p.lse[qrow] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+  } else {
+    const size_t slot = qrow * p.max_splits + s;
+    float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kD + c8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (c8 == 0) {
+      p.ws_md[slot * 2] = M;
+      p.ws_md[slot * 2 + 1] = W;
     }
   }
 }
@@ -411,20 +402,12 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
 
 size_t decode_smem_bytes() { return kRingBytes + 2 * kStages * 8 + 16 + 1024; }
 
-template <int R>
-static cudaError_t configure_one() {
-  // Prefer shared memory over L1 so four CTAs' rings fit on an SM.
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<R>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_split_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)decode_smem_bytes());
-}
-
 cudaError_t decode_configure() {
-  cudaError_t e = configure_one<1>();
-  if (e == cudaSuccess) e = configure_one<2>();
-  if (e == cudaSuccess) e = configure_one<4>();
-  return e;
+  // Prefer shared memory over L1 so four CTAs' rings fit on an SM.
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)decode_smem_bytes());
 }
 int decode_threads() { return kThreads; }
 
@@ -435,13 +418,7 @@ namespace sa {
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                           cudaStream_t stream) {
   dim3 grid(p.max_splits, p.hkv, p.batch);
-  const int rows = p.group * p.q_len;
-  if (rows <= 16)
-    decode_split_kernel<1><<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
-  else if (rows <= 32)
-    decode_split_kernel<2><<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
-  else
-    decode_split_kernel<4><<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
+  decode_split_kernel<<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.direct) return e;
   const long long warps = (long long)p.batch * p.q_len * p.hq;

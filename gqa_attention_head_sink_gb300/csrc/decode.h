@@ -20,7 +20,9 @@ struct DecodeParams {
   float* ws_md;               // [B, q_len, Hq, max_splits, 2] partial (m, d), m in log2 units
   unsigned* err;              // device error word
   int batch, hq, hkv, group, stride;
-  int q_len;        // new query tokens per sequence (the last q_len of its cache); group * q_len <= 64
+  int q_len;            // new query tokens per sequence (the last q_len of its cache)
+  int tokens_per_tile;  // tensor-core kernel: new tokens per 128-row tile (tile rows = group * tokens_per_tile)
+  int row_tiles;        // tensor-core kernel: tiles per sequence, ceil(q_len / tokens_per_tile)
   int num_splits;   // > 0: requested chunks per sequence; 0: by length
   int split_pages;  // pages per chunk when num_splits == 0
   int max_splits;   // grid extent of the chunk dimension
@@ -43,10 +45,15 @@ __host__ __device__ inline int decode_num_chunks(int npages, int num_splits, int
   return (npages + chunk - 1) / chunk;
 }
 
-template <int R>
 __global__ void decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                                     const DecodeParams p);
 __global__ void decode_merge_kernel(const DecodeParams p);
+
+// Tensor-core variant for many query rows per kv head (multi-token decode):
+// 128-row tiles of (new token, query head) pairs, S and O in TMEM.
+__global__ void decode_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                                 const __grid_constant__ CUtensorMap vmap, const DecodeParams p);
+constexpr int kDecodeTcRows = 128;  // query rows of one tensor-core tile
 
 size_t decode_smem_bytes();
 
@@ -57,5 +64,10 @@ int decode_threads();
 // Enqueue the chunk kernel and, when chunks are merged, the merge kernel.
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                           cudaStream_t stream);
+// Same with the tensor-core chunk kernel (qmap: q as [B * q_len, Hq, 64],
+// boxes of group heads x tokens_per_tile tokens).
+cudaError_t decode_tc_configure();
+cudaError_t launch_decode_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace sa

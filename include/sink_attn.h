@@ -154,9 +154,13 @@ size_t sink_attn_decode_workspace_bytes(int batch, int max_seqlen, int num_q_hea
  *   q       bf16 [batch, q_len, num_q_heads, head_dim]
  *   out     [batch, q_len, num_q_heads, head_dim], bf16 or fp32 per out_dtype
  *   lse     optional fp32 [batch, q_len, num_q_heads]; NULL to skip
- *   q_len   >= 1, with (num_q_heads / num_kv_heads) * q_len <= 64 (the query
- *           rows that share one kv head are processed together, so every
- *           page is read once for all of them); e.g. q_len <= 8 at group 8.
+ *   q_len   1 .. 4096.  The query rows that share one kv head (group x
+ *           q_len) are processed together, so every page is read once for
+ *           all of them: up to 16 rows with warp-level MMAs, more on the
+ *           tensor cores in tiles of 128 (new token, query head) rows, which
+ *           also skip the key tiles no row of a tile can see.  Limits:
+ *           num_q_heads / num_kv_heads <= 16 and batch x ceil(q_len /
+ *           floor(128 / group)) <= 65535.
  *   workspace
  *           at least sink_attn_decode_multi_workspace_bytes(...) bytes,
  *           256-byte aligned, or NULL (allocated in stream order).

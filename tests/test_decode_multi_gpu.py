@@ -1,12 +1,14 @@
 """GPU parity of multi-token decode against the float64 oracle.
 
 q_len new tokens per sequence are the last q_len tokens of its paged cache:
-token t sits at position L - q_len + t and sees keys 0..L - q_len + t.  The
-kernel keeps every query row that reads one kv head (group x q_len rows, in
-tiles of 16) in one CTA, so the cases cover 1, 2, 3 and 4 row tiles, groups
-of 1, 4, 8 and 16, sequences shorter than q_len (tokens before the cache
-start see only the sink), sequences that are all new, ragged tails with
-poisoned slots, and every chunking.  All calls go through the C ABI.
+token t sits at position L - q_len + t and sees keys 0..L - q_len + t.  Up
+to 16 query rows per kv head (group x q_len) run on the warp-level-MMA split
+kernel, more on the tensor-core kernel in tiles of 128 (new token, head)
+rows.  The cases cover both kernels, one and several row tiles, groups of 1,
+4, 8 and 16, sequences shorter than q_len (tokens before the cache start see
+only the sink), sequences that are all new, long runs of new tokens against
+a cached prefix, ragged tails with poisoned slots, and every chunking.  All
+calls go through the C ABI.
 """
 import numpy as np
 import pytest
@@ -49,16 +51,20 @@ def oracle_multi(inp, seqs=None):
 
 SMALL = [
     # lengths, q_len, Hq, Hkv, sink mode, splits      (rows per kv head = Hq/Hkv * q_len)
-    ([1, 2, 15, 16, 17, 100, 333], 2, 64, 8, "normal2", 0),     # 16 rows: one tile
+    ([1, 2, 15, 16, 17, 100, 333], 2, 64, 8, "normal2", 0),     # 16 rows: warp-level MMAs
     ([1, 2, 15, 16, 17, 100, 333], 2, 64, 8, "normal2", 3),
-    ([0, 1, 3, 5, 2048, 1999], 4, 64, 8, "mixed", 0),           # 32 rows: two tiles; L < q_len
-    ([0, 5, 2048, 1999], 8, 64, 8, "mixed", 7),                 # 64 rows: four tiles
+    ([300, 31], 5, 8, 8, "zero", 2),                            # group 1: 5 rows
+    ([0, 1, 3, 5, 2048, 1999], 4, 64, 8, "mixed", 0),           # 32 rows: tensor cores; L < q_len
+    ([0, 5, 2048, 1999], 8, 64, 8, "mixed", 7),                 # 64 rows
     ([4000, 17, 1], 3, 16, 1, "mixed", 0),                      # group 16: 48 rows
     ([777, 778, 779, 780], 4, 16, 1, "normal1", 5),             # group 16: 64 rows
-    ([300, 31], 5, 8, 8, "zero", 2),                            # group 1: 5 rows
     ([5000], 8, 64, 8, "normal2", 256),                         # one page per chunk
     ([129] * 9, 6, 24, 3, "normal2", 0),                        # 48 rows
     ([16, 32, 48], 16, 16, 4, "neginf", 1),                     # q_len 16 x group 4; first sequence all new
+    ([1, 100, 4000], 16, 64, 8, "mixed", 0),                    # 128 rows: one full tile
+    ([50, 700, 3000], 40, 64, 8, "normal2", 0),                 # three row tiles (16 + 16 + 8 tokens)
+    ([300, 1000], 12, 32, 2, "normal2", 3),                     # group 16: two row tiles (8 + 4 tokens)
+    ([129, 260], 33, 8, 8, "normal1", 2),                       # group 1: 33 rows
 ]
 
 
@@ -116,14 +122,25 @@ def test_decode_multi_with_caller_workspace():
     assert_parity(out, want)
 
 
-def test_decode_multi_rejects_too_many_rows():
-    inp = workloads.make_decode([64], seed=35, q_len=9, device="cuda")
+def test_decode_multi_new_tokens_against_cached_prefix():
+    # 1000 new tokens per sequence after prefixes of 500 and 1100 cached ones:
+    # 63 row tiles per sequence and kv head, causal skipping of key tiles
+    inp = workloads.make_decode([1500, 2100], seed=36, sink_mode="mixed", q_len=1000, num_splits=0,
+                                spare_pages=2, poison=True, device="cuda")
+    out, lse = run(inp, with_lse=True)
+    want, want_lse = oracle_multi(inp)
+    assert_parity(out, want)
+    lse_close(lse, want_lse)
+
+
+def test_decode_multi_rejects_too_many_tokens():
+    inp = workloads.make_decode([4097], seed=35, q_len=4097, num_q_heads=8, num_kv_heads=8, device="cuda")
     with pytest.raises(sa.SinkAttnError) as e:
         run(inp)
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("q_len", [2, 4, 8])
+@pytest.mark.parametrize("q_len", [2, 4, 8, 16])
 def test_decode_multi_full_size_sampled(q_len):
     # batch 64 x 8192 cached tokens, 8 chunks: the shape of the decode benchmark
     inp = workloads.make_decode([8192] * 64, seed=2, sink_mode="normal2", num_splits=8, q_len=q_len,

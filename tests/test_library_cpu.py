@@ -157,8 +157,8 @@ def _decode_multi_call(lib, q_len, **kw):
 @pytest.mark.parametrize("q_len,kw,status", [
     (0, {}, 1),                       # at least one new token
     (-3, {}, 1),
-    (9, {}, 2),                       # 8 heads x 9 tokens = 72 rows share a kv head: more than 64
-    (5, dict(hq=64, hkv=4), 2),       # 16 x 5 = 80 rows
+    (4097, {}, 2),                    # at most 4096 new tokens per call
+    (2048, dict(batch=600), 2),       # 600 sequences x 128 row tiles: beyond the grid
     (4, dict(hq=64, hkv=2), 2),       # group of 32: beyond one row block per head group
     (2, dict(d=128), 2),
     (2, dict(q=8 * 16 + 8), 1),       # misaligned
