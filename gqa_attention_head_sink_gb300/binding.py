@@ -37,6 +37,9 @@ EXPORTS = {
                                       _P]),
     "sink_attn_decode_multi": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I,
                                     _P, _P, _SZ, _P]),
+    "sink_attn_prefill_paged": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I,
+                                     _P, _I, _P, _P, _SZ, _P]),
+    "sink_attn_prefill_paged_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "sink_attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "sink_attn_decode_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "sink_attn_decode_max_splits": (_I, [_I, _I, _I, _I, _I]),
@@ -248,6 +251,61 @@ def sink_attn_decode_multi(q, k_pages, v_pages, page_table, seqlens, sinks, scal
                                        OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse), ws_ptr,
                                        ws_bytes, _stream_ptr(stream))
     _check(st, "sink_attn_decode_multi")
+    return out
+
+
+def sink_attn_prefill_paged_workspace_bytes(batch: int, total_q: int, max_seqlen_q: int, max_seqlen_k: int,
+                                            num_q_heads: int, num_kv_heads: int, head_dim: int = 64,
+                                            page_size: int = 16, num_splits: int = 0) -> int:
+    n = load().sink_attn_prefill_paged_workspace_bytes(batch, total_q, max_seqlen_q, max_seqlen_k, num_q_heads,
+                                                       num_kv_heads, head_dim, page_size, num_splits)
+    if n == ctypes.c_size_t(-1).value:
+        raise SinkAttnError(1, "sink_attn_prefill_paged_workspace_bytes")
+    return n
+
+
+def sink_attn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqlens_k, sinks, scale: float,
+                            num_splits: int = 0, out=None, out_dtype=torch.float32, lse=None,
+                            max_seqlen_q: Optional[int] = None, max_seqlen_k: Optional[int] = None,
+                            workspace=None, stream=None):
+    """Chunked prefill against the paged cache.  q [total_q,Hq,64] bf16 packed
+    by cu_seqlens_q [B+1] int32: the new tokens of sequence b are the last
+    n_b of its seqlens_k[b] cached tokens (token t at position L - n_b + t,
+    causal).  Other arguments as sink_attn_decode.  Returns out
+    [total_q,Hq,64]."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(seqlens_k, "seqlens_k", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    total_q, hq, d = q.shape
+    num_pages, hkv, page_size, d2 = k_pages.shape
+    B = seqlens_k.shape[0]
+    if v_pages.shape != k_pages.shape or d2 != d:
+        raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
+    if page_table.shape[0] != B or cu_seqlens_q.shape[0] != B + 1:
+        raise ValueError("page_table needs one row and cu_seqlens_q one offset per sequence (plus one)")
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B > 0 else 0
+    if max_seqlen_k is None:
+        max_seqlen_k = int(seqlens_k.max().item()) if B > 0 else 0
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=out_dtype, device=q.device)
+    _need(out, "out", out.dtype, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = load().sink_attn_prefill_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                        page_table.shape[1], _ptr(cu_seqlens_q), _ptr(seqlens_k), B, total_q,
+                                        int(max_seqlen_q), int(max_seqlen_k), num_pages, _ptr(sinks), hq, hkv, d,
+                                        page_size, float(scale), int(num_splits), _ptr(out),
+                                        OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse), ws_ptr,
+                                        ws_bytes, _stream_ptr(stream))
+    _check(st, "sink_attn_prefill_paged")
     return out
 
 

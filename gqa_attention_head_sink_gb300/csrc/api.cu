@@ -141,19 +141,25 @@ struct DecodePlan {
 };
 
 // Rows of one tensor-core decode tile are (new token, query head) pairs of one
-// kv head: this many tokens per tile, and this many tiles per sequence.
-int decode_tokens_per_tile(int group, int q_len) { return std::max(1, std::min(q_len, kDecodeTcRows / group)); }
-int decode_row_tiles(int group, int q_len) {
-  if (group * q_len < kTensorCoreMinRows) return 1;
-  const int tpt = decode_tokens_per_tile(group, q_len);
-  return (q_len + tpt - 1) / tpt;
+// kv head: this many tokens per tile, and this many tiles per sequence
+// (max_q = the most new tokens any sequence has).
+int decode_tokens_per_tile(int group, int max_q) { return std::max(1, std::min(max_q, kDecodeTcRows / group)); }
+int decode_row_tiles(int group, int max_q, bool tensor_cores) {
+  if (!tensor_cores) return 1;
+  const int tpt = decode_tokens_per_tile(group, max_q);
+  return std::max(1, (max_q + tpt - 1) / tpt);
 }
+bool decode_uses_tensor_cores(int group, int q_len) { return group * q_len >= kTensorCoreMinRows; }
 
-bool plan_decode(int batch, int q_len, int max_seqlen, int num_q_heads, int num_kv_heads, int num_splits,
-                 DecodePlan* pl) {
-  if (batch < 0 || q_len <= 0 || max_seqlen < 0 || num_kv_heads <= 0 || num_q_heads <= 0) return false;
+// Chunking of the key length.  num_splits > 0: that many chunks per sequence.
+// 0: chunks of 16..128 pages aiming at kDecodeTargetCtas CTAs; when the row
+// tiles alone give that many CTAs (long runs of new tokens), the chunks grow
+// past 128 pages so that the key length is not split needlessly.
+bool plan_decode(int batch, int max_q, long long total_q, int max_seqlen, int num_q_heads, int num_kv_heads,
+                 int num_splits, bool tensor_cores, DecodePlan* pl) {
+  if (batch < 0 || max_q < 0 || total_q < 0 || max_seqlen < 0 || num_kv_heads <= 0 || num_q_heads <= 0) return false;
   if (num_q_heads % num_kv_heads) return false;
-  const int row_tiles = decode_row_tiles(num_q_heads / num_kv_heads, q_len);
+  const int row_tiles = decode_row_tiles(num_q_heads / num_kv_heads, std::max(1, max_q), tensor_cores);
   if (num_splits < 0 || num_splits > kMaxSplits) return false;
   const long long max_pages = ((long long)max_seqlen + kPageSize - 1) / kPageSize;
   int split_pages = kMaxSplitPages;
@@ -163,7 +169,8 @@ bool plan_decode(int batch, int q_len, int max_seqlen, int num_q_heads, int num_
   } else {
     long long sp = ((long long)batch * row_tiles * num_kv_heads * max_pages + kDecodeTargetCtas - 1) /
                    kDecodeTargetCtas;
-    sp = std::min<long long>(kMaxSplitPages, std::max<long long>(kMinSplitPages, sp));
+    sp = std::max<long long>(kMinSplitPages, sp);
+    if (row_tiles == 1) sp = std::min<long long>(kMaxSplitPages, sp);
     if ((max_pages + sp - 1) / sp > kMaxSplits) sp = (max_pages + kMaxSplits - 1) / kMaxSplits;
     split_pages = (int)sp;
     max_splits = (int)std::max(1LL, (max_pages + sp - 1) / sp);
@@ -174,19 +181,29 @@ bool plan_decode(int batch, int q_len, int max_seqlen, int num_q_heads, int num_
   if (pl->direct) {
     pl->ws_bytes = 0;
   } else {
-    const size_t slots = (size_t)batch * q_len * num_q_heads * max_splits;
+    const size_t slots = (size_t)total_q * num_q_heads * max_splits;
     const size_t o_bytes = (slots * kHeadDim * 4 + 255) / 256 * 256;
     pl->ws_bytes = o_bytes + slots * 2 * 4;
   }
   return true;
 }
 
-// Shared body of sink_attn_decode (q_len = 1) and sink_attn_decode_multi.
+// Which query rows a paged call has: q_len new tokens per sequence (cu_q
+// null), or per-sequence counts from the device offsets cu_q [batch + 1].
+struct QueryLayout {
+  const int32_t* cu_q;
+  int q_len;    // uniform count when cu_q is null
+  int total_q;  // rows of q and out: batch * q_len, or cu_q[batch]
+  int max_q;    // no sequence has more new tokens than this
+};
+
+// Shared body of sink_attn_decode (q_len = 1), sink_attn_decode_multi and
+// sink_attn_prefill_paged.
 int decode_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
-                int page_table_stride, const int32_t* seqlens, int batch, int q_len, int max_seqlen, int num_pages,
-                const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale,
-                int num_splits, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
-                void* stream);
+                int page_table_stride, const int32_t* seqlens, int batch, const QueryLayout& ql, int max_seqlen,
+                int num_pages, const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream);
 
 }  // namespace
 }  // namespace sa
@@ -229,7 +246,7 @@ int sink_attn_get_device_error(void* stream) {
 int sink_attn_decode_max_splits(int batch, int max_seqlen, int num_kv_heads, int page_size, int num_splits) {
   if (page_size != kPageSize) return 0;
   DecodePlan pl;
-  if (!plan_decode(batch, 1, max_seqlen, num_kv_heads, num_kv_heads, num_splits, &pl)) return 0;
+  if (!plan_decode(batch, 1, batch, max_seqlen, num_kv_heads, num_kv_heads, num_splits, false, &pl)) return 0;
   return pl.max_splits;
 }
 
@@ -241,9 +258,22 @@ size_t sink_attn_decode_workspace_bytes(int batch, int max_seqlen, int num_q_hea
 
 size_t sink_attn_decode_multi_workspace_bytes(int batch, int q_len, int max_seqlen, int num_q_heads,
                                               int num_kv_heads, int head_dim, int page_size, int num_splits) {
+  if (head_dim != kHeadDim || page_size != kPageSize || q_len <= 0 || num_kv_heads <= 0) return (size_t)-1;
+  DecodePlan pl;
+  const bool tc = decode_uses_tensor_cores(num_q_heads / num_kv_heads, q_len);
+  if (!plan_decode(batch, q_len, (long long)batch * q_len, max_seqlen, num_q_heads, num_kv_heads, num_splits, tc,
+                   &pl))
+    return (size_t)-1;
+  return pl.ws_bytes;
+}
+
+size_t sink_attn_prefill_paged_workspace_bytes(int batch, int total_q, int max_seqlen_q, int max_seqlen_k,
+                                               int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                                               int num_splits) {
   if (head_dim != kHeadDim || page_size != kPageSize) return (size_t)-1;
   DecodePlan pl;
-  if (!plan_decode(batch, q_len, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl)) return (size_t)-1;
+  if (!plan_decode(batch, max_seqlen_q, total_q, max_seqlen_k, num_q_heads, num_kv_heads, num_splits, true, &pl))
+    return (size_t)-1;
   return pl.ws_bytes;
 }
 
@@ -252,7 +282,8 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
                      const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
                      float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
                      size_t workspace_bytes, void* stream) {
-  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, 1, max_seqlen, num_pages,
+  const QueryLayout ql{nullptr, 1, batch, 1};
+  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, ql, max_seqlen, num_pages,
                      sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out, out_dtype, lse,
                      workspace, workspace_bytes, stream);
 }
@@ -262,7 +293,25 @@ int sink_attn_decode_multi(const void* q, const void* k_pages, const void* v_pag
                            int num_pages, const float* sinks, int num_q_heads, int num_kv_heads, int head_dim,
                            int page_size, float scale, int num_splits, void* out, int out_dtype, float* lse,
                            void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, q_len, max_seqlen,
+  if (q_len <= 0) return SINK_ATTN_ERR_INVALID_ARG;
+  if ((long long)batch * q_len >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
+  const QueryLayout ql{nullptr, q_len, batch * q_len, q_len};
+  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, ql, max_seqlen, num_pages,
+                     sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out, out_dtype, lse,
+                     workspace, workspace_bytes, stream);
+}
+
+int sink_attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                            int page_table_stride, const int32_t* cu_seqlens_q, const int32_t* seqlens_k, int batch,
+                            int total_q, int max_seqlen_q, int max_seqlen_k, int num_pages, const float* sinks,
+                            int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale,
+                            int num_splits, void* out, int out_dtype, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_q > total_q) return SINK_ATTN_ERR_INVALID_ARG;
+  if (batch == 0 || total_q == 0) return SINK_ATTN_OK;
+  if (!cu_seqlens_q || !aligned16(cu_seqlens_q)) return SINK_ATTN_ERR_INVALID_ARG;
+  const QueryLayout ql{cu_seqlens_q, 0, total_q, max_seqlen_q};
+  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens_k, batch, ql, max_seqlen_k,
                      num_pages, sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out,
                      out_dtype, lse, workspace, workspace_bytes, stream);
 }
@@ -273,12 +322,12 @@ namespace sa {
 namespace {
 
 int decode_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
-                int page_table_stride, const int32_t* seqlens, int batch, int q_len, int max_seqlen, int num_pages,
-                const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale,
-                int num_splits, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
-                void* stream) {
+                int page_table_stride, const int32_t* seqlens, int batch, const QueryLayout& ql, int max_seqlen,
+                int num_pages, const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream) {
   // ---- validation (nothing is enqueued on failure)
-  if (batch < 0 || q_len <= 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+  if (batch < 0 || ql.max_q < 0 || ql.total_q < 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
     return SINK_ATTN_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads) return SINK_ATTN_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > kMaxSplits) return SINK_ATTN_ERR_INVALID_ARG;
@@ -286,10 +335,11 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   if (!(scale > 0.f) || !std::isfinite(scale)) return SINK_ATTN_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || page_size != kPageSize) return SINK_ATTN_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > kMaxGroupDecode) return SINK_ATTN_ERR_UNSUPPORTED;
-  if (q_len > kMaxDecodeTokens) return SINK_ATTN_ERR_UNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
-  const bool tensor_cores = group * q_len >= kTensorCoreMinRows;
-  const int row_tiles = decode_row_tiles(group, q_len);
+  // per-sequence counts (paged prefill) always take the tensor-core kernel
+  const bool tensor_cores = ql.cu_q != nullptr || decode_uses_tensor_cores(group, ql.q_len);
+  if (!ql.cu_q && ql.q_len > kMaxDecodeTokens) return SINK_ATTN_ERR_UNSUPPORTED;
+  const int row_tiles = decode_row_tiles(group, std::max(1, ql.max_q), tensor_cores);
   if (batch == 0) return SINK_ATTN_OK;
   if (!q || !k_pages || !v_pages || !page_table || !seqlens || !sinks || !out) return SINK_ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(page_table) ||
@@ -298,10 +348,11 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   if (num_pages <= 0 || page_table_stride <= 0) return SINK_ATTN_ERR_INVALID_ARG;
   if ((long long)page_table_stride * kPageSize < max_seqlen) return SINK_ATTN_ERR_INVALID_ARG;
   if ((long long)batch * row_tiles > 65535 || num_kv_heads > 65535) return SINK_ATTN_ERR_UNSUPPORTED;
-  if ((long long)batch * q_len * num_q_heads >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)ql.total_q * num_q_heads >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
   if ((long long)num_pages * num_kv_heads * kPageSize >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
   DecodePlan pl;
-  if (!plan_decode(batch, q_len, max_seqlen, num_q_heads, num_kv_heads, num_splits, &pl))
+  if (!plan_decode(batch, std::max(1, ql.max_q), ql.total_q, max_seqlen, num_q_heads, num_kv_heads, num_splits,
+                   tensor_cores, &pl))
     return SINK_ATTN_ERR_INVALID_ARG;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SINK_ATTN_ERR_INVALID_ARG;
   if (workspace && workspace_bytes < pl.ws_bytes) return SINK_ATTN_ERR_INVALID_ARG;
@@ -322,10 +373,10 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   CUtensorMap kmap, vmap;
   if ((st = encode_rows64(&kmap, k_pages, rows, kHeadDim * 2, kPageSize))) return st;
   if ((st = encode_rows64(&vmap, v_pages, rows, kHeadDim * 2, kPageSize))) return st;
-  const int tokens_per_tile = decode_tokens_per_tile(group, q_len);
-  CUtensorMap qmap;  // tensor-core path: q as [batch * q_len tokens, Hq, 64], one box = one row tile
+  const int tokens_per_tile = decode_tokens_per_tile(group, std::max(1, ql.max_q));
+  CUtensorMap qmap;  // tensor-core path: q as [total_q tokens, Hq, 64], one box = one row tile
   if (tensor_cores &&
-      (st = encode_tokens_heads(&qmap, q, (uint64_t)batch * q_len, num_q_heads, tokens_per_tile, group)))
+      (st = encode_tokens_heads(&qmap, q, (uint64_t)ql.total_q, num_q_heads, tokens_per_tile, group)))
     return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -346,7 +397,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   p.out = out;
   p.lse = lse;
   if (pl.ws_bytes) {
-    const size_t slots = (size_t)batch * q_len * num_q_heads * pl.max_splits;
+    const size_t slots = (size_t)ql.total_q * num_q_heads * pl.max_splits;
     p.ws_o = static_cast<float*>(ws);
     p.ws_md = reinterpret_cast<float*>(static_cast<char*>(ws) + (slots * kHeadDim * 4 + 255) / 256 * 256);
   }
@@ -356,7 +407,9 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   p.hkv = num_kv_heads;
   p.group = num_q_heads / num_kv_heads;
   p.stride = page_table_stride;
-  p.q_len = q_len;
+  p.q_len = ql.q_len;
+  p.cu_q = ql.cu_q;
+  p.total_q = ql.total_q;
   p.tokens_per_tile = tokens_per_tile;
   p.row_tiles = row_tiles;
   p.num_splits = num_splits;

@@ -361,14 +361,25 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   }
 }
 
-// Combine the chunks' partial states: one warp per (sequence, new token,
-// query head) row.  Lane l owns output dims 2l, 2l+1.  Chunk c contributes
-// with weight 2^(m_c - M), M = max_c m_c; chunks that saw nothing have
-// m_c = -inf.
+// Combine the chunks' partial states: one warp per (row of q, query head).
+// Lane l owns output dims 2l, 2l+1.  Chunk c contributes with weight
+// 2^(m_c - M), M = max_c m_c; chunks that saw nothing have m_c = -inf.
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  const int b = wid / (p.hq * p.q_len);
-  if (b >= p.batch) return;
+  if (wid >= p.total_q * p.hq) return;
+  const int row = wid / p.hq;
+  int b;
+  if (p.cu_q) {  // the last sequence whose new tokens start at or before this row
+    int lo = 0, hi = p.batch;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.cu_q[mid] <= row) lo = mid;
+      else hi = mid;
+    }
+    b = lo;
+  } else {
+    b = row / p.q_len;
+  }
   const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
   int n, pg0, pg1;
   chunk_range(p, L, 0, n, pg0, pg1);
@@ -421,7 +432,7 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   decode_split_kernel<<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.direct) return e;
-  const long long warps = (long long)p.batch * p.q_len * p.hq;
+  const long long warps = (long long)p.total_q * p.hq;
   decode_merge_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -10,17 +10,19 @@
 namespace sa {
 
 struct DecodeParams {
-  const __nv_bfloat16* q;     // [B, q_len, Hq, 64]
+  const __nv_bfloat16* q;     // [total_q, Hq, 64]: [B, q_len, Hq, 64] or packed by cu_q
   const int32_t* page_table;  // [B, stride]
   const int32_t* seqlens;     // [B]
   const float* sinks;         // [Hq]
-  void* out;                  // [B, q_len, Hq, 64] bf16 or fp32
-  float* lse;                 // [B, q_len, Hq] or null
-  float* ws_o;                // [B, q_len, Hq, max_splits, 64] partial weighted sums
-  float* ws_md;               // [B, q_len, Hq, max_splits, 2] partial (m, d), m in log2 units
+  void* out;                  // [total_q, Hq, 64] bf16 or fp32
+  float* lse;                 // [total_q, Hq] or null
+  float* ws_o;                // [total_q, Hq, max_splits, 64] partial weighted sums
+  float* ws_md;               // [total_q, Hq, max_splits, 2] partial (m, d), m in log2 units
   unsigned* err;              // device error word
   int batch, hq, hkv, group, stride;
-  int q_len;            // new query tokens per sequence (the last q_len of its cache)
+  int q_len;            // new query tokens per sequence (the last q_len of its cache), when cu_q is null
+  const int32_t* cu_q;  // tensor-core kernel: [B + 1] offsets of each sequence's new tokens, or null
+  int total_q;          // rows of q / out: B * q_len, or cu_q[B]
   int tokens_per_tile;  // tensor-core kernel: new tokens per 128-row tile (tile rows = group * tokens_per_tile)
   int row_tiles;        // tensor-core kernel: tiles per sequence, ceil(q_len / tokens_per_tile)
   int num_splits;   // > 0: requested chunks per sequence; 0: by length

@@ -11,8 +11,9 @@
 // heads of the group for tokens_per_tile consecutive new tokens, row
 // rho = t_local * G + (h mod G).  That is exactly how a 3-D TMA box of
 // (64 dims, G heads, tokens_per_tile tokens) lands in shared memory, so Q is
-// one copy.  New token t of a sequence with L cached tokens sees keys
-// 0 .. L - q_len + t.
+// one copy.  A sequence with L cached tokens has n new ones (the last n of
+// the cache: q_len each, or from the offsets cu_q for a paged prefill); new
+// token t sees keys 0 .. L - n + t.
 //
 // Per key tile of 128 tokens (8 pages):
 //   * warp 0 (producer): one 2 KiB TMA copy per page for K and for V (the
@@ -84,6 +85,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   const int s = blockIdx.x, g = blockIdx.y;
   const int b = blockIdx.z / p.row_tiles, tile = blockIdx.z % p.row_tiles;
+  int q0 = b * p.q_len, nq = p.q_len;  // first row of q and number of new tokens of the sequence
+  if (p.cu_q) {                        // offsets are device data: clamp them to the rows of q
+    q0 = min(max(0, p.cu_q[b]), p.total_q);
+    nq = max(0, min(p.cu_q[b + 1], p.total_q) - q0);
+  }
+  const int G = p.group, tpt = p.tokens_per_tile;
+  const int t0 = tile * tpt;  // first new token of the tile
+  if (t0 >= nq) return;
   const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
   const int npages = (L + kPage - 1) / kPage;
   const int n_chunks = decode_num_chunks(npages, p.num_splits, p.split_pages, p.max_splits);
@@ -91,12 +100,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int chunk = npages > 0 ? (npages + n_chunks - 1) / n_chunks : 0;
   const int pg0 = s * chunk;
   const int pg1 = min(npages, pg0 + chunk);
-  const int G = p.group, tpt = p.tokens_per_tile;
-  const int t0 = tile * tpt;                          // first new token of the tile
-  const int t_last = min(p.q_len, t0 + tpt) - 1;      // last new token of the tile
-  const int box_rows = G * tpt;                       // rows the Q copy fills
+  const int t_last = min(nq, t0 + tpt) - 1;  // last new token of the tile
+  const int box_rows = G * tpt;              // rows the Q copy fills
   // keys [pg0*16, kend) of this chunk can be visible to some row of the tile
-  const int kend = min(min(L, pg1 * kPage), L - p.q_len + t_last + 1);
+  const int kend = min(min(L, pg1 * kPage), L - nq + t_last + 1);
   const int nkeys = max(0, kend - pg0 * kPage);
   const int ntiles = (nkeys + kKeyTile - 1) / kKeyTile;
 
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint64_t pol_stream = l2_policy_evict_first();
     if (ntiles > 0 && !p.withhold_copies && elect_one()) {  // no copy may outlive the CTA: Q only if used
       mbar_arrive_expect_tx(q_full, box_rows * kD * 2);
-      tma_load_3d(q_tile, &qmap, q_full, 0, g * G, b * p.q_len + t0);
+      tma_load_3d(q_tile, &qmap, q_full, 0, g * G, q0 + t0);
     }
     const int32_t* row = p.page_table + (size_t)b * p.stride;
     uint32_t ring_i = 0;
@@ -251,9 +258,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int t_loc = r / G;
       const int t = t0 + t_loc;                        // new token of the row
       const int h = g * G + (r - t_loc * G);           // query head of the row
-      const bool row_ok = r < box_rows && t < p.q_len;
+      const bool row_ok = r < box_rows && t < nq;
       // keys visible to this row, relative to the chunk start
-      const int lim = (row_ok ? min(kend, L - p.q_len + t + 1) : kend) - pg0 * kPage;
+      const int lim = (row_ok ? min(kend, L - nq + t + 1) : kend) - pg0 * kPage;
       const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
       const uint32_t s_addr = tmem + lane_off + kColS;
       const uint32_t p_addr = tmem + lane_off + kColP;
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int e = 0; e < 64; ++e) ob[e] = 0u;  // no key in this chunk: O = 0
       }
       if (ok && row_ok) {
-        const size_t qrow = ((size_t)b * p.q_len + t) * p.hq + h;  // (sequence, token, head)
+        const size_t qrow = ((size_t)q0 + t) * p.hq + h;  // (row of q, head)
         if (p.direct) {
           const float inv = d > 0.f ? 1.f / d : 0.f;
           if (p.out_f32) {
@@ -395,7 +402,7 @@ cudaError_t launch_decode_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, c
   decode_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.direct) return e;
-  const long long warps = (long long)p.batch * p.q_len * p.hq;
+  const long long warps = (long long)p.total_q * p.hq;
   decode_merge_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

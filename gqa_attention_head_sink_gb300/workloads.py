@@ -77,6 +77,9 @@ class DecodeInputs:
     scale: float
     num_splits: int            # 0 = chosen per length by the library
     page_size: int = PAGE_SIZE
+    # chunked prefill: q is [total_q, Hq, D], packed by these offsets [B+1]
+    cu_seqlens_q: Optional[torch.Tensor] = None
+    q_lens: Optional[List[int]] = None
 
     @property
     def batch(self) -> int:
@@ -93,6 +96,8 @@ class DecodeInputs:
     @property
     def q_len(self) -> int:
         """New query tokens per sequence (1 for a [B, Hq, D] query)."""
+        if self.q_lens is not None:
+            raise ValueError("per-sequence new-token counts: see q_lens")
         return self.q.shape[1] if self.q.dim() == 4 else 1
 
     @property
@@ -103,7 +108,8 @@ class DecodeInputs:
         return dataclasses.replace(
             self, q=self.q.to(device), k_pages=self.k_pages.to(device),
             v_pages=self.v_pages.to(device), page_table=self.page_table.to(device),
-            seqlens_t=self.seqlens_t.to(device), sinks=self.sinks.to(device))
+            seqlens_t=self.seqlens_t.to(device), sinks=self.sinks.to(device),
+            cu_seqlens_q=None if self.cu_seqlens_q is None else self.cu_seqlens_q.to(device))
 
 
 def _generator(device, seed: int) -> torch.Generator:
@@ -157,7 +163,7 @@ def make_prefill(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, see
 def make_decode(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, seed=0,
                 sink_mode="normal2", scale: Optional[float] = None, num_splits=0,
                 page_size=PAGE_SIZE, spare_pages=0, poison=False, q_len: Optional[int] = None,
-                device="cpu") -> DecodeInputs:
+                q_lens: Optional[List[int]] = None, device="cpu") -> DecodeInputs:
     """Paged decode inputs: one bf16 query per sequence (q [B, Hq, D]), or
     ``q_len`` new query tokens per sequence (q [B, q_len, Hq, D]: the last
     q_len tokens of each sequence's cache), KV pool in pages of
@@ -165,7 +171,9 @@ def make_decode(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, seed
     table that maps each sequence's logical pages to a random permutation of
     the pool.  ``spare_pages`` adds pool pages that no sequence owns.  With
     ``poison`` the slots past each sequence's length in its last page and the
-    spare pages hold NaN, so any read beyond the valid tokens shows up."""
+    spare pages hold NaN, so any read beyond the valid tokens shows up.
+    ``q_lens`` (chunked prefill): per-sequence new-token counts instead; q is
+    then [sum(q_lens), Hq, D] packed by ``cu_seqlens_q``."""
     seqlens = [int(x) for x in seqlens]
     B = len(seqlens)
     pages_per_seq = [(L + page_size - 1) // page_size for L in seqlens]
@@ -173,7 +181,13 @@ def make_decode(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, seed
     num_pages = max(1, used + int(spare_pages))
     gen = _generator(device, seed)
     sinks = draw_sinks(num_q_heads, sink_mode, gen, device)
-    q_shape = (B, num_q_heads, head_dim) if q_len is None else (B, int(q_len), num_q_heads, head_dim)
+    if q_lens is not None:
+        q_lens = [int(x) for x in q_lens]
+        q_shape = (sum(q_lens), num_q_heads, head_dim)
+    elif q_len is None:
+        q_shape = (B, num_q_heads, head_dim)
+    else:
+        q_shape = (B, int(q_len), num_q_heads, head_dim)
     q = _randn_bf16(q_shape, gen, device)
     k_pages = _randn_bf16((num_pages, num_kv_heads, page_size, head_dim), gen, device)
     v_pages = _randn_bf16((num_pages, num_kv_heads, page_size, head_dim), gen, device)
@@ -199,9 +213,22 @@ def make_decode(seqlens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, seed
             k_pages[spare.long()] = nan
             v_pages[spare.long()] = nan
     lens_t = torch.tensor(seqlens, dtype=torch.int32, device=device)
+    cu_q = None
+    if q_lens is not None:
+        cu_q = torch.zeros(B + 1, dtype=torch.int32)
+        if B:
+            cu_q[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
+        cu_q = cu_q.to(device)
     return DecodeInputs(q=q, k_pages=k_pages, v_pages=v_pages, page_table=table, seqlens_t=lens_t,
                         seqlens=seqlens, sinks=sinks, num_splits=int(num_splits), page_size=page_size,
-                        scale=(1.0 / math.sqrt(head_dim)) if scale is None else float(scale))
+                        scale=(1.0 / math.sqrt(head_dim)) if scale is None else float(scale),
+                        cu_seqlens_q=cu_q, q_lens=q_lens)
+
+
+def make_paged_prefill(seqlens_k, new_lens, **kw) -> DecodeInputs:
+    """Chunked prefill inputs: sequence b holds seqlens_k[b] cached tokens in
+    its pages, the last new_lens[b] of which are new and have a query each."""
+    return make_decode(seqlens_k, q_lens=list(new_lens), **kw)
 
 
 def _uniform_lengths(n, lo, hi, seed) -> List[int]:

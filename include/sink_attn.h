@@ -184,6 +184,59 @@ size_t sink_attn_decode_multi_workspace_bytes(int batch, int q_len, int max_seql
                                               int num_splits);
 
 /*
+ * Chunked prefill against the paged KV cache: a run of new tokens per
+ * sequence, already appended to its paged cache, attends causally to the
+ * whole cache ("GPT-OSS on day 0", section Sink Attention; the same online
+ * softmax, sink counted once, in the first chunk of the key length when the
+ * keys are split).  This is how a long prompt is prefilled piece by piece, or
+ * new tokens are appended to a sequence that already has a cache.
+ *
+ * Sequence b has n_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens; they
+ * are the LAST n_b of its L_b = seqlens_k[b] cached tokens, so new token t
+ * (0-based) sits at position L_b - n_b + t and sees keys 0 .. L_b - n_b + t.
+ * n_b = L_b is plain causal prefill; n_b = 1 is decode.  New tokens placed
+ * before the cache start (n_b > L_b) see no key: out = 0, lse = sink.
+ *
+ *   q             bf16 [total_q, num_q_heads, head_dim], packed by cu_seqlens_q
+ *   k_pages, v_pages, page_table, page_table_stride, num_pages, sinks,
+ *   num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits
+ *                 as in sink_attn_decode
+ *   cu_seqlens_q  int32 [batch + 1], DEVICE: cu[0] = 0, non-decreasing,
+ *                 cu[batch] = total_q
+ *   seqlens_k     int32 [batch], DEVICE: cached tokens of each sequence, the
+ *                 new ones included
+ *   total_q, max_seqlen_q, max_seqlen_k
+ *                 host values: max_seqlen_q >= every n_b, max_seqlen_k >=
+ *                 every L_b and <= page_table_stride * page_size
+ *   out           [total_q, num_q_heads, head_dim], bf16 or fp32 per out_dtype
+ *   lse           optional fp32 [total_q, num_q_heads]; NULL to skip
+ *   workspace     at least sink_attn_prefill_paged_workspace_bytes(...)
+ *                 bytes (0 when no sequence's keys are split: with num_splits
+ *                 = 0 that is the case once the new tokens alone fill the
+ *                 GPU), 256-byte aligned, or NULL (allocated in stream order)
+ * Runs on the tensor cores in tiles of 128 (new token, query head) rows of
+ * one kv head; key tiles no row of a tile can see are skipped.
+ * Limits: num_q_heads / num_kv_heads <= 16; batch x ceil(max_seqlen_q /
+ * floor(128 / group)) <= 65535; total_q * num_q_heads < 2^31.
+ * batch == 0 or total_q == 0 is a no-op returning SINK_ATTN_OK.
+ */
+int sink_attn_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                            const int32_t* page_table, int page_table_stride,
+                            const int32_t* cu_seqlens_q, const int32_t* seqlens_k, int batch,
+                            int total_q, int max_seqlen_q, int max_seqlen_k, int num_pages,
+                            const float* sinks, int num_q_heads, int num_kv_heads, int head_dim,
+                            int page_size, float scale, int num_splits,
+                            void* out, int out_dtype, float* lse,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace sink_attn_prefill_paged needs; (size_t)-1 for arguments
+ * it would reject on size grounds. */
+size_t sink_attn_prefill_paged_workspace_bytes(int batch, int total_q, int max_seqlen_q,
+                                               int max_seqlen_k, int num_q_heads,
+                                               int num_kv_heads, int head_dim, int page_size,
+                                               int num_splits);
+
+/*
  * The largest number of chunks any sequence gets for these arguments
  * (the grid's chunk dimension); 0 for arguments sink_attn_decode would reject.
  */

@@ -179,3 +179,44 @@ def test_decode_multi_workspace(lib):
     assert sa.sink_attn_decode_multi_workspace_bytes(64, 4, 8192, 64, 8, 64, 16, 8) == slots * 64 * 4 + slots * 8
     with pytest.raises(sa.SinkAttnError):
         sa.sink_attn_decode_multi_workspace_bytes(64, 0, 8192, 64, 8, 64, 16, 8)
+
+
+def _prefill_paged_call(lib, **kw):
+    args = dict(q=8 * 16, k=8 * 32, v=8 * 48, table=8 * 64, stride=8, cu=8 * 72, seqlens=8 * 80, batch=2,
+                total_q=100, max_q=60, max_k=120, num_pages=16, sinks=8 * 96, hq=64, hkv=8, d=64, page=16,
+                scale=0.125, splits=0, out=8 * 112, out_dtype=1)
+    args.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731  (fake, never dereferenced)
+    return lib.sink_attn_prefill_paged(P(args["q"]), P(args["k"]), P(args["v"]), P(args["table"]), args["stride"],
+                                       P(args["cu"]), P(args["seqlens"]), args["batch"], args["total_q"],
+                                       args["max_q"], args["max_k"], args["num_pages"], P(args["sinks"]), args["hq"],
+                                       args["hkv"], args["d"], args["page"], args["scale"], args["splits"],
+                                       P(args["out"]), args["out_dtype"], None, None, 0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(max_q=101), 1),             # more new tokens in one sequence than in the batch
+    (dict(total_q=-1), 1),
+    (dict(cu=None), 1),
+    (dict(cu=8 * 72 + 4), 1),         # misaligned offsets
+    (dict(stride=7), 1),              # page table too narrow for max_seqlen_k
+    (dict(hq=64, hkv=2), 2),          # group of 32
+    (dict(d=128), 2),
+    (dict(batch=40000, total_q=4000000, max_q=2048), 2),  # 40000 x 128 row tiles: beyond the grid
+])
+def test_prefill_paged_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _prefill_paged_call(lib, **kw) == status
+
+
+def test_prefill_paged_empty_is_noop(lib):
+    assert _prefill_paged_call(lib, batch=0) == 0
+    assert _prefill_paged_call(lib, total_q=0, max_q=0, q=None, out=None) == 0
+
+
+def test_prefill_paged_workspace(lib):
+    # new tokens filling the GPU: the key length is not split, no workspace
+    assert sa.sink_attn_prefill_paged_workspace_bytes(1, 8192, 8192, 16384, 64, 8) == 0
+    # a few new tokens over long caches: split, partial state per (row, head, chunk)
+    n = sa.sink_attn_prefill_paged_workspace_bytes(4, 64, 16, 8192, 64, 8, 64, 16, 4)
+    slots = 64 * 64 * 4
+    assert n == slots * 64 * 4 + slots * 8
