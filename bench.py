@@ -86,6 +86,7 @@ def _kernel_hash(files):
 
 PREFILL_SOURCES = ["prefill.cu", "prefill.h", "tcgen05.cuh", "common.cuh"]
 DECODE_SOURCES = ["decode.cu", "decode.h", "common.cuh"]
+DECODE_TC_SOURCES = ["decode_tc.cu", "decode.h", "tcgen05.cuh", "common.cuh"]
 
 
 def _traffic(kernel: str, files):
@@ -245,10 +246,11 @@ def run_ours(args, dist, rank, world):
     e2e = None
     if rank == 0:
         e2e = _e2e(sa, pre, dec, dev, stream, args)
+    peaks, peak_src = _peaks()
+    next_rows = _next_rows(sa, dev, stream, flush, peaks, peak_src) if rank == 0 else None
 
     if rank != 0:
         return None
-    peaks, peak_src = _peaks()
     cpu = _cpu_baseline()
     line = {
         "metric": METRIC,
@@ -284,12 +286,81 @@ def run_ours(args, dist, rank, world):
                      "kernel": "prefill_kernel",
                      "peak_source": f"{peak_src} (cuBLAS bf16 burst)"},
         "e2e": e2e,
+        "next_rows": next_rows,
         "cpu_baseline": cpu,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
     }
     return line
+
+
+def _time_calls(fn, stream, flush=None, steps=20, warmup=3):
+    """Mean device time (ms) of `fn` over `steps` calls, each bracketed by
+    CUDA events on `stream`; `flush` (if given) is rewritten before each call,
+    outside the events."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [_events() for _ in range(steps)]
+    for i, (a, b) in enumerate(ev):
+        if flush is not None:
+            flush.fill_(float(i))
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def _next_rows(sa, dev, stream, flush, peaks, peak_src):
+    """The rows built beyond the hot path, each on its own synthetic workload:
+    multi-token decode (HBM bound) and chunked prefill against the paged
+    cache (tensor bound).  Timed per call (chunk kernel + merge kernel)."""
+    res = {}
+    mtp = workloads.workload("mtp_decode", device=dev)
+    out = torch.empty(mtp.q.shape, dtype=torch.bfloat16, device=dev)
+    need = sa.sink_attn_decode_multi_workspace_bytes(mtp.batch, mtp.q_len, mtp.max_seqlen, mtp.num_q_heads,
+                                                     mtp.num_kv_heads, 64, 16, mtp.num_splits)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def call_mtp():
+        sa.sink_attn_decode_multi(mtp.q, mtp.k_pages, mtp.v_pages, mtp.page_table, mtp.seqlens_t, mtp.sinks,
+                                  mtp.scale, num_splits=mtp.num_splits, out=out, max_seqlen=mtp.max_seqlen,
+                                  workspace=ws)
+
+    ms = _time_calls(call_mtp, stream)  # 1 GiB of K/V: larger than L2, no flush needed
+    nb = workloads.decode_bytes(mtp.seqlens, mtp.num_q_heads, mtp.num_kv_heads, out_bytes=2, q_len=mtp.q_len)
+    gbs = nb / (ms * 1e-3) / 1e9
+    res["multi_token_decode"] = {
+        "workload": workloads.WORKLOADS["mtp_decode"], "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 4),
+        "bytes_per_launch": nb, "kernels": "decode_tc_kernel + decode_merge_kernel",
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "traffic": _traffic("decode_tc_kernel", DECODE_TC_SOURCES),
+                     "peak_source": f"{peak_src} (STREAM-style copy)"}}
+    del mtp, out, ws
+    cp = workloads.workload("chunked_prefill", device=dev)
+    out = torch.empty(cp.q.shape, dtype=torch.bfloat16, device=dev)
+
+    def call_cp():
+        sa.sink_attn_prefill_paged(cp.q, cp.k_pages, cp.v_pages, cp.page_table, cp.cu_seqlens_q, cp.seqlens_t,
+                                   cp.sinks, cp.scale, num_splits=cp.num_splits, out=out,
+                                   max_seqlen_q=max(cp.q_lens), max_seqlen_k=cp.max_seqlen)
+
+    ms = _time_calls(call_cp, stream, flush=flush)  # 96 MiB of inputs would stay in L2
+    fl = workloads.paged_prefill_flops(cp.seqlens, cp.q_lens, cp.num_q_heads)
+    tf = fl / (ms * 1e-3) / 1e12
+    res["chunked_prefill"] = {
+        "workload": workloads.WORKLOADS["chunked_prefill"], "value": round(tf, 3), "unit": "TFLOP/s",
+        "ms": round(ms, 4), "flops_per_launch": fl, "kernels": "decode_tc_kernel (keys not split: no merge)",
+        "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "traffic": _traffic("decode_tc_kernel", DECODE_TC_SOURCES),
+                     "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
+    del cp, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def _e2e(sa, pre, dec, dev, stream, args):

@@ -247,6 +247,10 @@ WORKLOADS = {
                    "lengths U[16384, 32768], sinks N(0,2), splits per length, seed 3",
     "ragged_prefill": "16 sequences, lengths U[256, 32768] packed by cu_seqlens, causal, Hq=64, "
                       "Hkv=8, D=64, sinks by head mod 4: -inf, 0, N(0,2), +20, seed 4",
+    "mtp_decode": "batch 64 x 8192 cached tokens, the last 4 of them new (4 queries each, causal among "
+                  "them), Hq=64, Hkv=8, D=64, paged KV (page 16), splits per length, sinks N(0,2), seed 5",
+    "chunked_prefill": "1 sequence, 8192 new tokens after an 8192-token cached prefix (16384 paged), causal, "
+                       "Hq=64, Hkv=8, D=64, splits per length, sinks N(0,2), seed 6",
 }
 
 
@@ -261,6 +265,10 @@ def workload_seqlens(name: str) -> List[int]:
         return _uniform_lengths(128, 16384, 32768, 3)
     if name == "ragged_prefill":
         return _uniform_lengths(16, 256, 32768, 4)
+    if name == "mtp_decode":
+        return [8192] * 64
+    if name == "chunked_prefill":
+        return [16384]
     raise KeyError(name)
 
 
@@ -287,6 +295,14 @@ def workload(name: str, device="cpu", **overrides):
         kw = dict(seed=4, sink_mode="mixed", scale=0.125)
         kw.update(overrides)
         return make_prefill(lens, device=device, **kw)
+    if name == "mtp_decode":
+        kw = dict(seed=5, sink_mode="normal2", scale=0.125, num_splits=0, q_len=4)
+        kw.update(overrides)
+        return make_decode(lens, device=device, **kw)
+    if name == "chunked_prefill":
+        kw = dict(seed=6, sink_mode="normal2", scale=0.125, num_splits=0)
+        kw.update(overrides)
+        return make_paged_prefill(lens, [8192], device=device, **kw)
     raise KeyError(name)
 
 
@@ -295,6 +311,17 @@ def prefill_flops(seqlens, num_q_heads, head_dim=HEAD_DIM) -> int:
     """4*D flop (QK^T and PV multiply-adds) per unmasked (query, key) pair per
     query head; causal: L(L+1)/2 pairs per sequence."""
     pairs = sum(L * (L + 1) // 2 for L in seqlens)
+    return 4 * head_dim * num_q_heads * pairs
+
+
+def paged_prefill_flops(seqlens_k, new_lens, num_q_heads, head_dim=HEAD_DIM) -> int:
+    """4*D flop per visible (query, key) pair per query head: new token t of
+    a sequence with L keys and n new tokens sees L - n + t + 1 keys."""
+    pairs = 0
+    for L, n in zip(seqlens_k, new_lens):
+        n_vis = min(n, L)  # tokens placed before the cache start see no key
+        last = L  # keys seen by the last new token
+        pairs += n_vis * last - n_vis * (n_vis - 1) // 2
     return 4 * head_dim * num_q_heads * pairs
 
 
