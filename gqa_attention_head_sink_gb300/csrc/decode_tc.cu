@@ -285,7 +285,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int vis = lim - j * kKeyTile;  // keys c < vis are visible
         float x[128];  // raw scores, -inf where masked
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = c < vis ? __uint_as_float(sr[c]) : -INFINITY;
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+        if (__any_sync(0xffffffffu, vis < kKeyTile)) {  // only tiles that cross a row's last key
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= vis) x[c] = -INFINITY;
+        }
         float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
         for (int c = 4; c < 124; c += 8) {
