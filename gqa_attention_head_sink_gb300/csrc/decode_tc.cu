@@ -84,7 +84,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   const int s = blockIdx.x, g = blockIdx.y;
-  const int b = blockIdx.z / p.row_tiles, tile = blockIdx.z % p.row_tiles;
+  // blockIdx.z = r * batch + b with tile = row_tiles - 1 - r: the last tiles of
+  // every sequence (which see the most keys) are launched first
+  const int b = blockIdx.z % p.batch, tile = p.row_tiles - 1 - (int)(blockIdx.z / p.batch);
   int q0 = b * p.q_len, nq = p.q_len;  // first row of q and number of new tokens of the sequence
   if (p.cu_q) {                        // offsets are device data: clamp them to the rows of q
     q0 = min(max(0, p.cu_q[b]), p.total_q);
