@@ -15,3 +15,4 @@ from .sink_attention import (  # noqa: F401
     prefill_rows,
     sink_softmax_rows,
 )
+from .rope import qkv_bias_rope, rope, yarn_inv_freq  # noqa: F401
