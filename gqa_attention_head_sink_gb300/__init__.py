@@ -1,8 +1,10 @@
 """GB300-native grouped-query attention with a per-head attention sink.
 
 Python face of the C-ABI library libsink_attn.so (see include/sink_attn.h):
-causal variable-length prefill, split-KV paged decode, multi-token decode
-and chunked prefill (new tokens per sequence against the paged cache).  The functions only
+causal variable-length prefill, split-KV paged decode, multi-token decode,
+chunked prefill (new tokens per sequence against the paged cache), and the
+QKV bias + YaRN rotary pass that prepares q, k and v (and appends k and v to
+the cache).  The functions only
 marshal torch tensors into the C calls; all the arithmetic runs in the CUDA
 kernels, and a missing library is an error, never a fallback.
 """
@@ -21,6 +23,8 @@ from .binding import (  # noqa: F401
     sink_attn_prefill,
     sink_attn_prefill_paged,
     sink_attn_prefill_paged_workspace_bytes,
+    sink_attn_qkv_rope,
     sink_attn_status_string,
     sink_attn_version,
+    sink_attn_yarn_inv_freq,
 )

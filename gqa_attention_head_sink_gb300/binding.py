@@ -43,6 +43,9 @@ EXPORTS = {
     "sink_attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "sink_attn_decode_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "sink_attn_decode_max_splits": (_I, [_I, _I, _I, _I, _I]),
+    "sink_attn_qkv_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P]),
+    "sink_attn_yarn_inv_freq": (_I, [_I, ctypes.c_double, ctypes.c_double, _I, ctypes.c_double, ctypes.c_double,
+                                     ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "sink_attn_status_string": (ctypes.c_char_p, [_I]),
     "sink_attn_get_device_error": (_I, [_P]),
     "sink_attn_version": (_I, []),
@@ -307,6 +310,53 @@ def sink_attn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqle
                                         ws_bytes, _stream_ptr(stream))
     _check(st, "sink_attn_prefill_paged")
     return out
+
+
+def sink_attn_yarn_inv_freq(head_dim: int = 64, base: float = 10000.0, factor: float = 1.0,
+                            original_max_position: int = 4096, beta_fast: float = 32.0, beta_slow: float = 1.0):
+    """YaRN rotary frequencies (host computation in the library).  Returns
+    (inv_freq as a CPU float32 tensor [head_dim / 2], attn_factor)."""
+    if head_dim <= 0 or head_dim % 2:
+        raise SinkAttnError(1, "sink_attn_yarn_inv_freq")
+    buf = (ctypes.c_float * (head_dim // 2))()
+    af = ctypes.c_float()
+    st = load().sink_attn_yarn_inv_freq(head_dim, float(base), float(factor), int(original_max_position),
+                                        float(beta_fast), float(beta_slow), buf, ctypes.byref(af))
+    _check(st, "sink_attn_yarn_inv_freq")
+    return torch.tensor(list(buf), dtype=torch.float32), float(af.value)
+
+
+def sink_attn_qkv_rope(q, k, v, positions, inv_freq, attn_factor: float = 1.0, q_bias=None, k_bias=None,
+                       v_bias=None, slot_mapping=None, k_pages=None, v_pages=None, stream=None):
+    """In place: q <- rot(q + q_bias), k <- rot(k + k_bias), v <- v + v_bias,
+    rotation by positions[t] * inv_freq (half-split planes) times attn_factor.
+    q [T,Hq,64], k/v [T,Hkv,64] bf16; biases [H,64] bf16 or None; positions [T]
+    int32; inv_freq [32] fp32 (CUDA).  With slot_mapping [T] int32 the new k/v
+    are also written to k_pages/v_pages [num_pages,Hkv,16,64] at those slots."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(positions, "positions", torch.int32, 1)
+    _need(inv_freq, "inv_freq", torch.float32, 1)
+    for name, b in (("q_bias", q_bias), ("k_bias", k_bias), ("v_bias", v_bias)):
+        if b is not None:
+            _need(b, name, torch.bfloat16, 2)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if k.shape != v.shape or k.shape[0] != T or positions.shape[0] != T or inv_freq.shape[0] != d // 2:
+        raise ValueError("q [T,Hq,D], k and v [T,Hkv,D], positions [T], inv_freq [D/2]")
+    num_pages, page_size = 0, 16
+    if slot_mapping is not None:
+        _need(slot_mapping, "slot_mapping", torch.int32, 1)
+        _need(k_pages, "k_pages", torch.bfloat16, 4)
+        _need(v_pages, "v_pages", torch.bfloat16, 4)
+        num_pages, page_size = k_pages.shape[0], k_pages.shape[2]
+    st = load().sink_attn_qkv_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(q_bias), _ptr(k_bias), _ptr(v_bias),
+                                   _ptr(positions), _ptr(inv_freq), float(attn_factor), T, hq, hkv, d,
+                                   _ptr(slot_mapping), _ptr(k_pages), _ptr(v_pages), num_pages, page_size,
+                                   _stream_ptr(stream))
+    _check(st, "sink_attn_qkv_rope")
+    return q, k, v
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -15,6 +15,7 @@
 #include "../../include/sink_attn.h"
 #include "decode.h"
 #include "prefill.h"
+#include "rope.h"
 
 namespace sa {
 
@@ -429,6 +430,71 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
 }  // namespace sa
 
 extern "C" {
+
+int sink_attn_yarn_inv_freq(int head_dim, double base, double factor, int original_max_position, double beta_fast,
+                            double beta_slow, float* inv_freq, float* attn_factor) {
+  if (!inv_freq || !attn_factor || head_dim <= 0 || head_dim % 2) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!(base > 1.0) || !std::isfinite(base) || !(factor > 0.0) || !std::isfinite(factor))
+    return SINK_ATTN_ERR_INVALID_ARG;
+  if (factor > 1.0 && (original_max_position <= 0 || !(beta_fast > beta_slow) || !(beta_slow > 0.0)))
+    return SINK_ATTN_ERR_INVALID_ARG;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double theta = std::pow(base, -2.0 * i / head_dim);
+    double f = theta;
+    if (factor > 1.0) {
+      // turns of this plane over the original context decide between keeping
+      // the frequency (many turns) and dividing it by the factor (< 1 turn)
+      const double turns = original_max_position * theta / two_pi;
+      const double ramp = std::min(1.0, std::max(0.0, (turns - beta_slow) / (beta_fast - beta_slow)));
+      f = (1.0 - ramp) * theta / factor + ramp * theta;
+    }
+    inv_freq[i] = (float)f;
+  }
+  *attn_factor = factor > 1.0 ? (float)(0.1 * std::log(factor) + 1.0) : 1.0f;
+  return SINK_ATTN_OK;
+}
+
+int sink_attn_qkv_rope(void* q, void* k, void* v, const void* q_bias, const void* k_bias, const void* v_bias,
+                       const int32_t* positions, const float* inv_freq, float attn_factor, int num_tokens,
+                       int num_q_heads, int num_kv_heads, int head_dim, const int32_t* slot_mapping,
+                       void* k_pages, void* v_pages, int num_pages, int page_size, void* stream) {
+  if (num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0) return SINK_ATTN_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(attn_factor)) return SINK_ATTN_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return SINK_ATTN_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return SINK_ATTN_OK;
+  if (!q || !k || !v || !positions || !inv_freq) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(positions) || !aligned16(inv_freq) ||
+      (q_bias && !aligned16(q_bias)) || (k_bias && !aligned16(k_bias)) || (v_bias && !aligned16(v_bias)))
+    return SINK_ATTN_ERR_INVALID_ARG;
+  if (slot_mapping) {
+    if (!aligned16(slot_mapping) || !k_pages || !v_pages || !aligned16(k_pages) || !aligned16(v_pages))
+      return SINK_ATTN_ERR_INVALID_ARG;
+    if (num_pages <= 0) return SINK_ATTN_ERR_INVALID_ARG;
+    if (page_size != kPageSize) return SINK_ATTN_ERR_UNSUPPORTED;
+  }
+  if ((long long)num_tokens * num_q_heads >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
+  RopeParams p{};
+  p.q = static_cast<__nv_bfloat16*>(q);
+  p.k = static_cast<__nv_bfloat16*>(k);
+  p.v = static_cast<__nv_bfloat16*>(v);
+  p.q_bias = static_cast<const __nv_bfloat16*>(q_bias);
+  p.k_bias = static_cast<const __nv_bfloat16*>(k_bias);
+  p.v_bias = static_cast<const __nv_bfloat16*>(v_bias);
+  p.positions = positions;
+  p.inv_freq = inv_freq;
+  p.attn_factor = attn_factor;
+  p.slot_mapping = slot_mapping;
+  p.k_pages = static_cast<__nv_bfloat16*>(k_pages);
+  p.v_pages = static_cast<__nv_bfloat16*>(v_pages);
+  p.num_pages = num_pages;
+  p.page_size = kPageSize;
+  p.tokens = num_tokens;
+  p.hq = num_q_heads;
+  p.hkv = num_kv_heads;
+  return launch_qkv_rope(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
+}
 
 int sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks, const int32_t* cu_seqlens,
                       int batch, int total_tokens, int max_seqlen, int num_q_heads, int num_kv_heads,

@@ -277,6 +277,60 @@ int sink_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_p
                              int page_size, float scale, int num_splits,
                              void* out, int out_dtype, float* lse, void* stream);
 
+/*
+ * QKV bias + rotary position encoding with YaRN frequencies, applied to the
+ * projections before attention ("GPT-OSS on day 0", model overview: YaRN
+ * positional encoding as in DeepSeek-V3, QKV projections with biases as in
+ * Qwen 2; the pages give no formula, the published definitions are used).
+ *
+ * In place, for every token t and head:
+ *   q[t,h] <- rot(q[t,h] + q_bias[h]),  k[t,g] <- rot(k[t,g] + k_bias[g]),
+ *   v[t,g] <- v[t,g] + v_bias[g]
+ * where rot rotates each plane (dim i, dim i + D/2) by the angle
+ * positions[t] * inv_freq[i] (computed without rounding: fp64 product, then
+ * reduced to [-pi, pi]) and multiplies the result by attn_factor; the sum
+ * and rotation run in fp32, the result is rounded once to bf16.
+ *
+ *   q, k, v     bf16 [num_tokens, H, head_dim] (H = num_q_heads for q,
+ *               num_kv_heads for k and v), DEVICE, modified in place
+ *   q_bias, k_bias, v_bias
+ *               bf16 [H, head_dim] DEVICE, or NULL for no bias
+ *   positions   int32 [num_tokens] DEVICE: position of each token in its
+ *               sequence (e.g. L - n + t for the n new tokens of a cache of L)
+ *   inv_freq    fp32 [head_dim / 2] DEVICE (sink_attn_yarn_inv_freq fills it)
+ *   attn_factor YaRN's temperature (sink_attn_yarn_inv_freq), 1 for plain RoPE
+ *   slot_mapping
+ *               optional int32 [num_tokens] DEVICE: cache slot (page *
+ *               page_size + offset) of each token; when given, the rotated k
+ *               and the biased v are also written to k_pages / v_pages
+ *               ([num_pages, num_kv_heads, page_size, head_dim] bf16) there.
+ *               Slots < 0 or past the pool are skipped.  NULL: no cache write.
+ * Limits: head_dim == 64, page_size == 16, num_tokens * num_q_heads < 2^31.
+ * num_tokens == 0 is a no-op returning SINK_ATTN_OK.
+ */
+int sink_attn_qkv_rope(void* q, void* k, void* v, const void* q_bias, const void* k_bias,
+                       const void* v_bias, const int32_t* positions, const float* inv_freq,
+                       float attn_factor, int num_tokens, int num_q_heads, int num_kv_heads,
+                       int head_dim, const int32_t* slot_mapping, void* k_pages, void* v_pages,
+                       int num_pages, int page_size, void* stream);
+
+/*
+ * YaRN rotary frequencies (host computation, no GPU): for plane i the base
+ * frequency theta_i = base^(-2i/head_dim); with factor s > 1 each plane's
+ * number of turns over the original context, r = original_max_position *
+ * theta_i / (2 pi), sets a ramp g = clamp((r - beta_slow) / (beta_fast -
+ * beta_slow), 0, 1) and the frequency becomes (1 - g) theta_i / s + g theta_i
+ * (YaRN's "NTK-by-parts" interpolation, linear in r as the YaRN paper writes
+ * it); attn_factor = 0.1 ln(s) + 1.  s <= 1 gives plain RoPE and 1.
+ *   inv_freq     HOST fp32 [head_dim / 2], written
+ *   attn_factor  HOST fp32, written
+ * Returns SINK_ATTN_ERR_INVALID_ARG for odd head_dim, base <= 1, factor <= 0,
+ * or (factor > 1) original_max_position <= 0 or not 0 < beta_slow < beta_fast.
+ */
+int sink_attn_yarn_inv_freq(int head_dim, double base, double factor, int original_max_position,
+                            double beta_fast, double beta_slow, float* inv_freq,
+                            float* attn_factor);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* sink_attn_status_string(int status);
 

@@ -220,3 +220,52 @@ def test_prefill_paged_workspace(lib):
     n = sa.sink_attn_prefill_paged_workspace_bytes(4, 64, 16, 8192, 64, 8, 64, 16, 4)
     slots = 64 * 64 * 4
     assert n == slots * 64 * 4 + slots * 8
+
+
+def test_yarn_inv_freq_matches_the_oracle(lib):
+    import numpy as np
+    import oracle
+    for args in [(64, 150000.0, 32.0, 4096, 32.0, 1.0), (64, 10000.0, 1.0, 4096, 32.0, 1.0),
+                 (128, 500000.0, 8.0, 8192, 16.0, 2.0)]:
+        f, af = sa.sink_attn_yarn_inv_freq(*args)
+        want, want_af = oracle.yarn_inv_freq(*args)
+        np.testing.assert_allclose(f.numpy(), want, rtol=2.0 ** -24, atol=0)
+        assert abs(af - want_af) <= 2.0 ** -23 * want_af
+
+
+@pytest.mark.parametrize("args", [(63, 1e4, 2.0, 4096, 32.0, 1.0), (64, 1.0, 2.0, 4096, 32.0, 1.0),
+                                  (64, 1e4, 0.0, 4096, 32.0, 1.0), (64, 1e4, 2.0, 0, 32.0, 1.0),
+                                  (64, 1e4, 2.0, 4096, 1.0, 32.0)])
+def test_yarn_inv_freq_rejects_bad_arguments(lib, args):
+    with pytest.raises(sa.SinkAttnError):
+        sa.sink_attn_yarn_inv_freq(*args)
+
+
+def _rope_call(lib, **kw):
+    args = dict(q=8 * 16, k=8 * 32, v=8 * 48, qb=None, kb=None, vb=None, pos=8 * 64, freq=8 * 80, af=1.0, T=10,
+                hq=8, hkv=2, d=64, slots=None, kp=None, vp=None, npages=0, page=16)
+    args.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731  (fake, never dereferenced)
+    return lib.sink_attn_qkv_rope(P(args["q"]), P(args["k"]), P(args["v"]), P(args["qb"]), P(args["kb"]),
+                                  P(args["vb"]), P(args["pos"]), P(args["freq"]), args["af"], args["T"], args["hq"],
+                                  args["hkv"], args["d"], P(args["slots"]), P(args["kp"]), P(args["vp"]),
+                                  args["npages"], args["page"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=128), 2),
+    (dict(hq=6, hkv=4), 1),
+    (dict(pos=None), 1),
+    (dict(freq=8 * 80 + 4), 1),        # misaligned
+    (dict(qb=8 * 96 + 8), 1),
+    (dict(af=float("inf")), 1),
+    (dict(slots=8 * 112), 1),          # cache write without pages
+    (dict(slots=8 * 112, kp=8 * 128, vp=8 * 144, npages=4, page=32), 2),
+    (dict(T=-1), 1),
+])
+def test_qkv_rope_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _rope_call(lib, **kw) == status
+
+
+def test_qkv_rope_empty_is_noop(lib):
+    assert _rope_call(lib, T=0, q=None) == 0
