@@ -87,6 +87,7 @@ def _kernel_hash(files):
 PREFILL_SOURCES = ["prefill.cu", "prefill.h", "tcgen05.cuh", "common.cuh"]
 DECODE_SOURCES = ["decode.cu", "decode.h", "common.cuh"]
 DECODE_TC_SOURCES = ["decode_tc.cu", "decode.h", "tcgen05.cuh", "common.cuh"]
+ROPE_SOURCES = ["rope.cu", "rope.h", "common.cuh"]
 
 
 def _traffic(kernel: str, files):
@@ -295,15 +296,19 @@ def run_ours(args, dist, rank, world):
     return line
 
 
-def _time_calls(fn, stream, flush=None, steps=20, warmup=3):
+def _time_calls(fn, stream, flush=None, steps=20, warmup=3, prepare=None):
     """Mean device time (ms) of `fn` over `steps` calls, each bracketed by
-    CUDA events on `stream`; `flush` (if given) is rewritten before each call,
-    outside the events."""
+    CUDA events on `stream`; `prepare` (if given) runs and `flush` (if given)
+    is rewritten before each call, both outside the events."""
     for _ in range(warmup):
+        if prepare is not None:
+            prepare()
         fn()
     torch.cuda.synchronize()
     ev = [_events() for _ in range(steps)]
     for i, (a, b) in enumerate(ev):
+        if prepare is not None:
+            prepare()
         if flush is not None:
             flush.fill_(float(i))
         a.record(stream)
@@ -315,8 +320,9 @@ def _time_calls(fn, stream, flush=None, steps=20, warmup=3):
 
 def _next_rows(sa, dev, stream, flush, peaks, peak_src):
     """The rows built beyond the hot path, each on its own synthetic workload:
-    multi-token decode (HBM bound) and chunked prefill against the paged
-    cache (tensor bound).  Timed per call (chunk kernel + merge kernel)."""
+    multi-token decode (HBM bound), chunked prefill against the paged cache
+    (tensor bound) and the QKV bias + YaRN rotary pass (HBM bound).  Timed
+    per call (chunk kernel + merge kernel where there is one)."""
     res = {}
     mtp = workloads.workload("mtp_decode", device=dev)
     out = torch.empty(mtp.q.shape, dtype=torch.bfloat16, device=dev)
@@ -359,6 +365,31 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
                      "traffic": _traffic("decode_tc_kernel", DECODE_TC_SOURCES),
                      "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
     del cp, out
+    # QKV bias + YaRN rotary pass over the prefill's 8192 tokens (in place: the
+    # inputs are restored from a pristine copy before each call, then L2 flushed)
+    ro = workloads.make_qkv_rope(8192, device=dev)
+    pristine = (ro.q.clone(), ro.k.clone(), ro.v.clone())
+    f, af = sa.sink_attn_yarn_inv_freq(64, **workloads.YARN_SETTINGS)
+    f = f.to(dev)
+
+    def restore():
+        ro.q.copy_(pristine[0])
+        ro.k.copy_(pristine[1])
+        ro.v.copy_(pristine[2])
+
+    def call_rope():
+        sa.sink_attn_qkv_rope(ro.q, ro.k, ro.v, ro.positions, f, af, ro.q_bias, ro.k_bias, ro.v_bias)
+
+    ms = _time_calls(call_rope, stream, flush=flush, prepare=restore)
+    nb = workloads.qkv_rope_bytes(8192, 64, 8)
+    gbs = nb / (ms * 1e-3) / 1e9
+    res["qkv_rope"] = {
+        "workload": workloads.WORKLOADS["qkv_rope"], "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 4),
+        "bytes_per_launch": nb, "kernels": "qkv_rope_kernel",
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": _traffic("qkv_rope_kernel", ROPE_SOURCES),
+                     "peak_source": f"{peak_src} (STREAM-style copy)"}}
+    del ro, pristine
     torch.cuda.empty_cache()
     return res
 

@@ -251,7 +251,47 @@ WORKLOADS = {
                   "them), Hq=64, Hkv=8, D=64, paged KV (page 16), splits per length, sinks N(0,2), seed 5",
     "chunked_prefill": "1 sequence, 8192 new tokens after an 8192-token cached prefix (16384 paged), causal, "
                        "Hq=64, Hkv=8, D=64, splits per length, sinks N(0,2), seed 6",
+    "qkv_rope": "8192 tokens (positions 0..8191), Hq=64, Hkv=8, D=64, q/k/v N(0,1), biases 0.5*N(0,1), all bf16; "
+                "YaRN base 150000, factor 32, original context 4096, beta_fast 32, beta_slow 1, seed 7",
 }
+
+# YaRN settings of the rotary workload: those of the public gpt-oss model
+# configuration (the pages name YaRN but give no parameters).
+YARN_SETTINGS = dict(base=150000.0, factor=32.0, original_max_position=4096, beta_fast=32.0, beta_slow=1.0)
+
+
+@dataclasses.dataclass
+class RopeInputs:
+    q: torch.Tensor          # [T, Hq, D] bf16
+    k: torch.Tensor          # [T, Hkv, D] bf16
+    v: torch.Tensor          # [T, Hkv, D] bf16
+    q_bias: torch.Tensor     # [Hq, D] bf16
+    k_bias: torch.Tensor     # [Hkv, D] bf16
+    v_bias: torch.Tensor     # [Hkv, D] bf16
+    positions: torch.Tensor  # [T] int32
+
+
+def make_qkv_rope(num_tokens, num_q_heads=64, num_kv_heads=8, head_dim=HEAD_DIM, seed=7, positions=None,
+                  device="cpu") -> RopeInputs:
+    """Inputs of the QKV bias + rotary pass: q/k/v ~ N(0,1) and biases
+    0.5 * N(0,1), rounded once to bf16; positions 0..T-1 unless given."""
+    gen = _generator(device, seed)
+    q = _randn_bf16((num_tokens, num_q_heads, head_dim), gen, device)
+    k = _randn_bf16((num_tokens, num_kv_heads, head_dim), gen, device)
+    v = _randn_bf16((num_tokens, num_kv_heads, head_dim), gen, device)
+    half = lambda *shape: (0.5 * torch.randn(*shape, generator=gen, device=device)).to(torch.bfloat16)  # noqa: E731
+    bq, bk, bv = half(num_q_heads, head_dim), half(num_kv_heads, head_dim), half(num_kv_heads, head_dim)
+    if positions is None:
+        positions = torch.arange(num_tokens, dtype=torch.int32, device=device)
+    return RopeInputs(q=q, k=k, v=v, q_bias=bq, k_bias=bk, v_bias=bv,
+                      positions=torch.as_tensor(positions, dtype=torch.int32, device=device))
+
+
+def qkv_rope_bytes(num_tokens, num_q_heads, num_kv_heads, head_dim=HEAD_DIM) -> int:
+    """Bytes the rotary pass must move: q, k, v read and written once (bf16),
+    the positions, and the biases."""
+    qkv = num_tokens * (num_q_heads + 2 * num_kv_heads) * head_dim * 2
+    return 2 * qkv + num_tokens * 4 + (num_q_heads + 2 * num_kv_heads) * head_dim * 2
 
 
 def workload_seqlens(name: str) -> List[int]:

@@ -44,3 +44,9 @@ def test_decode_bytes_count_each_kv_byte_once():
     kv = 64 * 8192 * 8 * 64 * 2 * 2
     q = o = 64 * 4 * 64 * 64 * 2
     assert n == kv + q + o + 64 * 512 * 4 + 64 * 4
+
+
+def test_qkv_rope_inputs_and_bytes():
+    r = workloads.make_qkv_rope(10, num_q_heads=8, num_kv_heads=2)
+    assert r.q.shape == (10, 8, 64) and r.k_bias.shape == (2, 64) and r.positions.tolist() == list(range(10))
+    assert workloads.qkv_rope_bytes(10, 8, 2) == 2 * 10 * 12 * 64 * 2 + 40 + 12 * 64 * 2
