@@ -343,7 +343,7 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
         "bytes_per_launch": nb, "kernels": "decode_tc_kernel + decode_merge_kernel",
         "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "traffic": _traffic("decode_tc_kernel", DECODE_TC_SOURCES),
+                     "traffic": _traffic("decode_tc_kernel/mtp_decode", DECODE_TC_SOURCES),
                      "peak_source": f"{peak_src} (STREAM-style copy)"}}
     del mtp, out, ws
     cp = workloads.workload("chunked_prefill", device=dev)
@@ -362,7 +362,7 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
         "ms": round(ms, 4), "flops_per_launch": fl, "kernels": "decode_tc_kernel (keys not split: no merge)",
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(tf / peaks["bf16_tflops"], 4),
-                     "traffic": _traffic("decode_tc_kernel", DECODE_TC_SOURCES),
+                     "traffic": _traffic("decode_tc_kernel/chunked_prefill", DECODE_TC_SOURCES),
                      "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
     del cp, out
     # QKV bias + YaRN rotary pass over the prefill's 8192 tokens (in place: the
