@@ -198,6 +198,13 @@ struct QueryLayout {
   int max_q;    // no sequence has more new tokens than this
 };
 
+// Chunked prefill on the persistent prefill kernel (paged mode).
+int prefill_paged_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                       int page_table_stride, const int32_t* cu_seqlens_q, const int32_t* seqlens_k, int batch,
+                       int total_q, int max_seqlen_q, int max_seqlen_k, int num_pages, const float* sinks,
+                       int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale, void* out,
+                       int out_dtype, float* lse, void* stream);
+
 // Shared body of sink_attn_decode (q_len = 1), sink_attn_decode_multi and
 // sink_attn_prefill_paged.
 int decode_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
@@ -275,6 +282,8 @@ size_t sink_attn_prefill_paged_workspace_bytes(int batch, int total_q, int max_s
   DecodePlan pl;
   if (!plan_decode(batch, max_seqlen_q, total_q, max_seqlen_k, num_q_heads, num_kv_heads, num_splits, true, &pl))
     return (size_t)-1;
+  // the same choice as sink_attn_prefill_paged: the persistent prefill kernel splits nothing
+  if (num_splits == 0 && max_seqlen_q >= kPrefillTileRows && batch <= kPrefillMaxBatch) return 0;
   return pl.ws_bytes;
 }
 
@@ -311,6 +320,13 @@ int sink_attn_prefill_paged(const void* q, const void* k_pages, const void* v_pa
   if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_q > total_q) return SINK_ATTN_ERR_INVALID_ARG;
   if (batch == 0 || total_q == 0) return SINK_ATTN_OK;
   if (!cu_seqlens_q || !aligned16(cu_seqlens_q)) return SINK_ATTN_ERR_INVALID_ARG;
+  // Runs of at least a query tile of new tokens: the persistent prefill kernel
+  // in paged mode (two heads per CTA sharing each K/V tile).  Shorter runs, or
+  // a requested split of the key length: the tensor-core decode kernel.
+  if (num_splits == 0 && max_seqlen_q >= kPrefillTileRows && batch <= kPrefillMaxBatch)
+    return prefill_paged_impl(q, k_pages, v_pages, page_table, page_table_stride, cu_seqlens_q, seqlens_k, batch,
+                              total_q, max_seqlen_q, max_seqlen_k, num_pages, sinks, num_q_heads, num_kv_heads,
+                              head_dim, page_size, scale, out, out_dtype, lse, stream);
   const QueryLayout ql{cu_seqlens_q, 0, total_q, max_seqlen_q};
   return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens_k, batch, ql, max_seqlen_k,
                      num_pages, sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out,
@@ -496,6 +512,81 @@ int sink_attn_qkv_rope(void* q, void* k, void* v, const void* q_bias, const void
   return launch_qkv_rope(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace sa {
+namespace {
+
+int prefill_paged_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                       int page_table_stride, const int32_t* cu_seqlens_q, const int32_t* seqlens_k, int batch,
+                       int total_q, int max_seqlen_q, int max_seqlen_k, int num_pages, const float* sinks,
+                       int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale, void* out,
+                       int out_dtype, float* lse, void* stream) {
+  // ---- validation (nothing is enqueued on failure); same rules as the decode paths
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || max_seqlen_k < 0) return SINK_ATTN_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads) return SINK_ATTN_ERR_INVALID_ARG;
+  if (out_dtype != SINK_ATTN_OUT_BF16 && out_dtype != SINK_ATTN_OUT_F32) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return SINK_ATTN_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || page_size != kPageSize) return SINK_ATTN_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads > kMaxGroupDecode) return SINK_ATTN_ERR_UNSUPPORTED;
+  if (!q || !k_pages || !v_pages || !page_table || !seqlens_k || !sinks || !out) return SINK_ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(page_table) ||
+      !aligned16(seqlens_k) || !aligned16(sinks) || !aligned16(out) || (lse && !aligned16(lse)))
+    return SINK_ATTN_ERR_INVALID_ARG;
+  if (num_pages <= 0 || page_table_stride <= 0) return SINK_ATTN_ERR_INVALID_ARG;
+  if ((long long)page_table_stride * kPageSize < max_seqlen_k) return SINK_ATTN_ERR_INVALID_ARG;
+  if (max_seqlen_q >= (1 << 24) || num_kv_heads > 65535) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)total_q * num_q_heads >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
+  if ((long long)num_pages * num_kv_heads * kPageSize >= (1LL << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
+
+  int dev;
+  int st = current_device(&dev);
+  if (st) return st;
+  unsigned* err;
+  if ((st = error_word(dev, &err))) return st;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_prefill_attr_set[dev]) {
+      if (prefill_configure() != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+      g_prefill_attr_set[dev] = true;
+    }
+  }
+  const uint64_t rows = (uint64_t)num_pages * num_kv_heads * kPageSize;
+  CUtensorMap qmap, kmap, vmap;
+  if ((st = encode_tokens_heads(&qmap, q, total_q, num_q_heads, kPrefillTileRows))) return st;
+  if ((st = encode_rows64(&kmap, k_pages, rows, kHeadDim * 2, kPageSize))) return st;
+  if ((st = encode_rows64(&vmap, v_pages, rows, kHeadDim * 2, kPageSize))) return st;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SINK_ATTN_ERR_CUDA;
+
+  PrefillParams p{};
+  p.cu_seqlens = cu_seqlens_q;
+  p.sinks = sinks;
+  p.out = out;
+  p.lse = lse;
+  p.err = err;
+  p.batch = batch;
+  p.total_tokens = total_q;
+  p.hq = num_q_heads;
+  p.hkv = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.max_qblocks = (max_seqlen_q + kPrefillTileRows - 1) / kPrefillTileRows;
+  p.out_f32 = out_dtype == SINK_ATTN_OUT_F32;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = wait_limit_ns();
+  p.withhold_copies = withhold_copies();
+  p.kv_len = seqlens_k;
+  p.page_table = page_table;
+  p.stride = page_table_stride;
+  cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, true, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" {
+
 int sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks, const int32_t* cu_seqlens,
                       int batch, int total_tokens, int max_seqlen, int num_q_heads, int num_kv_heads,
                       int head_dim, float scale, void* out, int out_dtype, float* lse, void* stream) {
@@ -549,7 +640,7 @@ int sink_attn_prefill(const void* q, const void* k, const void* v, const float* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.withhold_copies = withhold_copies();
-  cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }
 

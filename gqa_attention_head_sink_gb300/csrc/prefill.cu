@@ -13,7 +13,7 @@
 //     blocks with the most key tiles first), the heads of one group adjacent so
 //     that concurrently running CTAs read the same K/V from L2, and dealt to
 //     CTAs in a serpentine order.
-//   * warp 0 (elected lane): TMA producer.  Loads the two 128x64 Q tiles of a
+//   * warp 2 (elected lane): TMA producer.  Loads the two 128x64 Q tiles of a
 //     unit, then K_0, V_0, K_1, V_1, ... through an 8-slot ring of 16 KiB
 //     tiles (128-byte swizzle), each slot guarded by a full/empty mbarrier.
 //   * warps 1 and 3: MMA issuers for head 0 and head 1.  S_t = Q_t K_j^T
@@ -27,7 +27,7 @@
 //     the causal mask on the diagonal tile, updates (m, d), and writes P (bf16)
 //     to its own TMEM columns once the previous tile's PV has finished with
 //     them; at the end it normalises O by d and stores the row.
-//   * warp 2 allocates / frees the 512 TMEM columns:
+//   * warp 0 allocates / frees the 512 TMEM columns:
 //       S_0 [0,128)  S_1 [128,256)  O_0 [256,320)  O_1 [320,384)  P_0 [384,448)  P_1 [448,512)
 //     P has two bf16 per column.  Keeping P apart from S means a QK MMA never
 //     waits for the PV MMA reading the previous P.
@@ -40,6 +40,17 @@
 // d accumulates the bf16-rounded P (the values the PV MMA multiplies), so the
 // rounding of P perturbs the weights of a convex combination of V rows
 // instead of scaling the output.
+//
+// Paged mode (template flag; chunked prefill against the paged KV cache): a
+// sequence's query rows are the last n of its L cached tokens, so row i sits
+// at position L - n + i and sees keys 0 .. L - n + i.  K/V tiles of 128 keys
+// are gathered as 8 page slabs (2 KiB TMA copies, 8 per tile); a unit needs
+// the key tiles up to its last row's position; the causal mask applies to
+// every tile that crosses a row's last key; rows may see no key at all (more
+// query rows than cached tokens), which the softmax guards; V rows past the
+// last needed key are zeroed before the last PV (stale or poisoned slots must
+// not meet a zero weight inside the MMA).  The contiguous path compiles
+// without any of it.
 #include "common.cuh"
 #include "prefill.h"
 #include "tcgen05.cuh"
@@ -55,6 +66,9 @@ constexpr int kD = 64;
 constexpr int kTileBytes = kTile * kD * 2;  // 16 KiB
 constexpr int kSlots = 8;
 constexpr int kThreads = 384;
+// Warp roles 0..3: the TMA producer sits on the scheduler (warp % 4) that has
+// no MMA issuer, so its copy instructions do not queue behind an issuer's.
+constexpr int kProducerWarp = 2, kTmemWarp = 0;
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }   // S_t
 __host__ __device__ constexpr uint32_t col_o(int t) { return t ? 320u : 256u; }  // O_t
@@ -70,7 +84,10 @@ constexpr int kOffBar = kOffRing + kSlots * kTileBytes;  // mbarriers
 constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBar + 256;
 constexpr int kOffSeq = kOffMisc + 64;
-constexpr int kSmemBytes = kOffSeq + 4 * kPrefillMaxBatch * 4 + 1024;
+constexpr int kSeqArrays = 6;
+constexpr int kSmemBytes = kOffSeq + kSeqArrays * kPrefillMaxBatch * 4 + 1024;
+constexpr int kPage = 16;
+constexpr int kSlabBytes = kPage * kD * 2;  // one (page, kv head) slab: 2 KiB
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
 struct Bars {
@@ -131,6 +148,12 @@ __device__ __forceinline__ bool next_unit(int k, int total, int pairs_per_group,
   return true;
 }
 
+// Paged mode: keys a unit needs, [0, kend): up to the position of its last
+// query row (may be <= 0 when every row sits before the cache start).
+__device__ __forceinline__ int paged_kend(int kv_len, int q_len, int qb) {
+  return kv_len - q_len + min(q_len, (qb + 1) * kTile);
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const PrefillParams& p,
                                               volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;  // fast path: already complete
@@ -142,6 +165,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 
 }  // namespace
 
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -161,10 +185,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* total_qblocks = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  // paged mode: tail-V zeroings head 0's MMA warp has finished (head 1's waits on the count,
+  // which cannot alias the way a phase bit could when head 0 runs a unit ahead)
+  volatile int* zeroed_count = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
   int* seq_start = reinterpret_cast<int*>(smem + kOffSeq);   // sorted
   int* seq_len = seq_start + kPrefillMaxBatch;                // sorted
   int* seq_nqb = seq_len + kPrefillMaxBatch;                  // sorted, descending
   int* tmp_nqb = seq_nqb + kPrefillMaxBatch;                  // by batch index
+  int* seq_kv = tmp_nqb + kPrefillMaxBatch;                   // sorted; paged mode: cached tokens
+  int* seq_id = seq_kv + kPrefillMaxBatch;                    // sorted; paged mode: batch index
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.batch;
@@ -189,9 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bars.drain, 2);
     *abort_flag = 0;
+    *zeroed_count = 0;
     fence_barrier_init();
   }
-  if (warp == 2) {
+  if (warp == kTmemWarp) {
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -209,6 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     seq_start[rank] = st;
     seq_len[rank] = max(0, __ldg(p.cu_seqlens + i + 1) - st);
     seq_nqb[rank] = mine;
+    if constexpr (kPaged) {
+      seq_kv[rank] = min(max(0, __ldg(p.kv_len + i)), p.stride * kPage);  // never past the page-table row
+      seq_id[rank] = i;
+    }
     if (i == 0) *total_qblocks = total;
   }
   tc_fence_after();
@@ -223,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_tile[2] = {smem + kOffQ, smem + kOffQ + kTileBytes};
   uint8_t* ring = smem + kOffRing;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ================================================================ TMA producer
     // The whole warp runs the loop and waits; one elected lane issues the copies.
     if (elect_one()) {
@@ -246,8 +280,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_hint(q_tile[1], &qmap, bars.q_full, 0, hB, t0, pol_stream);
       }
       const int kv0 = seq_start[u.seq];
-      const int n = u.qb + 1;
+      int n = u.qb + 1, kend = 0;
+      const int32_t* table_row = nullptr;
+      if constexpr (kPaged) {
+        kend = paged_kend(seq_kv[u.seq], seq_len[u.seq], u.qb);
+        n = max(1, (kend + kTile - 1) / kTile);  // at least one (possibly empty) tile: the unit still runs
+        table_row = p.page_table + (size_t)seq_id[u.seq] * p.stride;
+      }
+      // paged mode: this lane's page of the next tile, read one tile ahead so the
+      // page-table latency overlaps the current tile's copies
+      auto slabs = [&](int j) { return min(kTile / kPage, max(0, (kend - j * kTile + kPage - 1) / kPage)); };
+      int next_page = 0;
+      if constexpr (kPaged) next_page = lane < slabs(0) ? __ldg(table_row + lane) : 0;
       for (int j = 0; j < n && ok; ++j) {
+        int np = 0, page = 0;  // paged mode: slabs of this tile, and this lane's page
+        if constexpr (kPaged) {
+          np = slabs(j);
+          page = next_page;
+          if (j + 1 < n && lane < slabs(j + 1)) next_page = __ldg(table_row + (j + 1) * (kTile / kPage) + lane);
+        }
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
           const uint32_t slot = ring_i % kSlots;
@@ -255,9 +306,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               !(ok = __all_sync(0xffffffffu,
                                 wait_or_abort(bars.slot_empty + slot, ((ring_i / kSlots) - 1) & 1, p, abort_flag))))
             break;
-          if (!p.withhold_copies && elect_one()) {
-            mbar_arrive_expect_tx(bars.slot_full + slot, kTileBytes);
-            tma_load_3d(ring + slot * kTileBytes, kv ? &vmap : &kmap, bars.slot_full + slot, 0, u.g, kv0 + j * kTile);
+          if constexpr (kPaged) {
+            if (!p.withhold_copies) {
+              if (elect_one()) mbar_arrive_expect_tx(bars.slot_full + slot, np * kSlabBytes);
+              __syncwarp();
+              if (lane < np)
+                tma_load_2d(ring + slot * kTileBytes + lane * kSlabBytes, kv ? &vmap : &kmap, bars.slot_full + slot,
+                            0, (page * p.hkv + u.g) * kPage);
+            }
+          } else {
+            if (!p.withhold_copies && elect_one()) {
+              mbar_arrive_expect_tx(bars.slot_full + slot, kTileBytes);
+              tma_load_3d(ring + slot * kTileBytes, kv ? &vmap : &kmap, bars.slot_full + slot, 0, u.g,
+                          kv0 + j * kTile);
+            }
           }
           ++ring_i;
         }
@@ -285,10 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, abort_flag));
     };
     const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t), a_p = tmem + col_p(t);
+    int zeroings = 0;  // paged mode: tail-V zeroings met so far
     Unit u;
     bool ok = true;
     for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
-      const int n = u.qb + 1;
+      int n = u.qb + 1, kend = 0;
+      if constexpr (kPaged) {
+        kend = paged_kend(seq_kv[u.seq], seq_len[u.seq], u.qb);
+        n = max(1, (kend + kTile - 1) / kTile);
+      }
       if (!(ok = wait_all(bars.q_full, k & 1))) break;
       // K_0 -> S (once the softmax has released S)
       if (!(ok = wait_all(bars.slot_full + ring_i % kSlots, (ring_i / kSlots) & 1))) break;
@@ -328,6 +395,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_all(bars.p_full + t, pph))) break;
         pph ^= 1;
         tc_fence_after();
+        if constexpr (kPaged) {
+          const int valid = kend - j * kTile;  // keys of this tile the unit needs
+          if (valid < kTile) {
+            // rows past them: slabs not copied or slots past the sequence end.  Head 0's
+            // warp zeroes them (fence for the tensor core's reads); head 1's waits for it.
+            ++zeroings;
+            if (t == 0) {
+              uint4* vrows = reinterpret_cast<uint4*>(ring + (vi % kSlots) * kTileBytes);
+              for (int i = max(0, valid) * 8 + lane; i < kTile * 8; i += 32) vrows[i] = make_uint4(0, 0, 0, 0);
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncwarp();
+              __threadfence_block();
+              if (lane == 0) *zeroed_count = zeroings;
+            } else {
+              bool seen = *zeroed_count >= zeroings;
+              const uint64_t t0 = seen ? 0 : global_timer_ns();
+              while (!seen && !*abort_flag) {
+                __nanosleep(64);
+                seen = *zeroed_count >= zeroings;
+                if (!seen && global_timer_ns() - t0 > p.wait_limit_ns) {
+                  atomicOr(p.err, kErrPrefill);
+                  *abort_flag = 1;
+                }
+              }
+              if (!(ok = __all_sync(0xffffffffu, seen))) break;
+              __threadfence_block();
+            }
+          }
+        }
         if (elect_one()) {
           const uint64_t dv = slot_desc(vi);
           if (j > 0) {
@@ -362,7 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit u;
     bool ok = true;
     for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
-      const int n = u.qb + 1;
+      int n = u.qb + 1;
+      int lim0 = 0;     // paged mode: keys visible to this row, counted from the unit's first key tile
+      int j_mask = 0;   // paged mode: first key tile that crosses the last key of some row of this warp
+      if constexpr (kPaged) {
+        const int kend = paged_kend(seq_kv[u.seq], seq_len[u.seq], u.qb);
+        n = max(1, (kend + kTile - 1) / kTile);
+        lim0 = seq_kv[u.seq] - seq_len[u.seq] + u.qb * kTile + r + 1;
+        j_mask = __reduce_min_sync(0xffffffffu, (unsigned)max(0, lim0) / kTile);
+      }
       const int h = u.g * p.group + 2 * u.pair + t;
       const bool head_ok = 2 * u.pair + t < p.group;
       float m = head_ok ? __ldg(p.sinks + h) * kLog2e : -INFINITY;  // sink-seeded state
@@ -381,10 +485,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        if (j == n - 1) {  // diagonal tile: key c is visible to row r iff c <= r
+        if constexpr (kPaged) {
+          if (j >= j_mask) {  // warp-uniform: the tiles before it are fully visible to every row
+            const int lim = lim0 - j * kTile;  // key c of this tile is visible iff c < lim
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > r) s[c] = -INFINITY;
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) s[c] = -INFINITY;
+          }
+        } else {
+          if (j == n - 1) {  // diagonal tile: key c is visible to row r iff c <= r
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > r) s[c] = -INFINITY;
+          }
         }
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
@@ -400,8 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = m_tile > m + kRescaleThreshold;
         const bool any_need = __any_sync(0xffffffffu, need);
         const float m_new = need ? m_tile : m;
-        const float alpha = fast_exp2(m - m_new);  // 1 unless this row's maximum moved
-        const float2 neg_m2 = make_float2(-m_new, -m_new);
+        // paged mode: a row may have seen neither sink nor key yet (-inf); subtract 0 then
+        const float m_ref = (kPaged && m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = fast_exp2(m - m_ref);  // 1 unless this row's maximum moved
+        const float2 neg_m2 = make_float2(-m_ref, -m_ref);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t pk[64];
 #pragma unroll
@@ -450,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row_tok = u.qb * kTile + r;
       const int tok = seq_start[u.seq] + row_tok;  // checked against T too: cu_seqlens is not trusted
       if (head_ok && row_tok < seq_len[u.seq] && tok >= 0 && tok < p.total_tokens) {
-        const float inv = 1.f / d;
+        const float inv = (!kPaged || d > 0.f) ? 1.f / d : 0.f;  // paged: no key and no sink gives 0
         const size_t row = (size_t)tok * p.hq + h;
         if (p.out_f32) {
           float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * kD);
@@ -470,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[i] = v;
           }
         }
-        if (p.lse) p.lse[row] = (m + __log2f(d)) * kLn2;
+        if (p.lse) p.lse[row] = (!kPaged || d > 0.f) ? (m + __log2f(d)) * kLn2 : -INFINITY;
       }
     }
   }
@@ -478,22 +593,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == kTmemWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 cudaError_t prefill_configure() {
-  return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const PrefillParams& p, int num_sms, cudaStream_t stream) {
+                           const PrefillParams& p, int num_sms, bool paged, cudaStream_t stream) {
   const long long ppg = (p.group + 1) / 2;
   const long long upper = ppg * p.hkv * ((long long)(p.total_tokens + kTile - 1) / kTile + p.batch);
   const int grid = (int)std::min<long long>(std::max(1, num_sms), std::max(1LL, upper));
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  if (paged)
+    prefill_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  else
+    prefill_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
 

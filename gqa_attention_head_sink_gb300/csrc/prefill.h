@@ -13,7 +13,7 @@ constexpr int kPrefillKeyRows = 128;    // keys per K/V tile
 constexpr int kPrefillMaxBatch = 1024;  // sequences per call (per-CTA schedule table)
 
 struct PrefillParams {
-  const int32_t* cu_seqlens;  // [B+1]
+  const int32_t* cu_seqlens;  // [B+1]: query rows of each sequence (contiguous mode: its keys too)
   const float* sinks;         // [Hq]
   void* out;                  // [T, Hq, 64] bf16 or fp32
   float* lse;                 // [T, Hq] or null
@@ -24,15 +24,24 @@ struct PrefillParams {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int withhold_copies;  // failure-path test: the producer issues no copies, so the waits time out
+  // Paged mode (chunked prefill against the paged KV cache): the keys of
+  // sequence b are its kv_len[b] cached tokens, read page by page, and its
+  // n_b query rows are the last n_b of them (row i at position
+  // kv_len[b] - n_b + i, causal).
+  const int32_t* kv_len;      // [B]
+  const int32_t* page_table;  // [B, stride]
+  int stride;
 };
 
 // One-time per-device kernel attributes (dynamic shared memory size).
 cudaError_t prefill_configure();
 
 // Enqueue the persistent prefill kernel: `grid_ctas` <= number of SMs.
-// qmap / kmap / vmap are 3-D maps over [T, heads, 64] with boxes of 128 (q) or
-// 64 (k, v) tokens x 1 head x 64 dims.
+// qmap is a 3-D map over [T, Hq, 64] with boxes of 128 tokens x 1 head x 64
+// dims.  Contiguous mode: kmap / vmap are the same over [T, Hkv, 64].  Paged
+// mode: 2-D maps over the pools viewed as [num_pages * Hkv * 16, 64] with
+// boxes of one (page, kv head) slab of 16 rows.
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const PrefillParams& p, int num_sms, cudaStream_t stream);
+                           const PrefillParams& p, int num_sms, bool paged, cudaStream_t stream);
 
 }  // namespace sa

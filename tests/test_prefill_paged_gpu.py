@@ -1,5 +1,9 @@
 """GPU parity of chunked prefill against the paged cache (float64 oracle).
 
+Runs of at least 128 new tokens (with the key length not split) take the
+persistent prefill kernel's paged mode; the others the tensor-core decode
+kernel; the cases below exercise both.
+
 Sequence b has n_b new tokens, the last n_b of its L_b cached ones; new token
 t sees keys 0 .. L_b - n_b + t.  Cases: prefixes of every length including
 none (plain causal prefill) and sequences with no new token, more new tokens
@@ -81,6 +85,23 @@ def test_prefill_paged_all_new_matches_contiguous_prefill():
                                max_seqlen=max(lens))
     torch.cuda.synchronize()
     assert_parity(out, ref.double().cpu().numpy())
+
+
+def test_prefill_paged_long_runs_equal_contiguous_prefill_bit_for_bit():
+    # runs of >= 128 new tokens go to the persistent prefill kernel's paged mode: with every
+    # token new it must give exactly what the contiguous prefill gives on the gathered cache
+    lens = [1000, 333, 4097]
+    inp = workloads.make_paged_prefill(lens, lens, seed=54, sink_mode="mixed", num_splits=0, spare_pages=2,
+                                       poison=True, device="cuda")
+    out, lse = run(inp, with_lse=True)
+    j = [torch.arange(L, device="cuda") for L in lens]
+    k = torch.cat([inp.k_pages[inp.page_table[b, jj // 16].long(), :, jj % 16] for b, jj in enumerate(j)])
+    v = torch.cat([inp.v_pages[inp.page_table[b, jj // 16].long(), :, jj % 16] for b, jj in enumerate(j)])
+    lse_ref = torch.empty_like(lse)
+    ref = sa.sink_attn_prefill(inp.q, k.contiguous(), v.contiguous(), inp.sinks, inp.cu_seqlens_q, inp.scale,
+                               max_seqlen=max(lens), lse=lse_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref) and torch.equal(lse, lse_ref)
 
 
 def test_prefill_paged_splits_agree():
