@@ -359,10 +359,11 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
     tf = fl / (ms * 1e-3) / 1e12
     res["chunked_prefill"] = {
         "workload": workloads.WORKLOADS["chunked_prefill"], "value": round(tf, 3), "unit": "TFLOP/s",
-        "ms": round(ms, 4), "flops_per_launch": fl, "kernels": "decode_tc_kernel (keys not split: no merge)",
+        "ms": round(ms, 4), "flops_per_launch": fl,
+        "kernels": "prefill_kernel, paged mode (runs of >= 128 new tokens, keys not split: no merge)",
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(tf / peaks["bf16_tflops"], 4),
-                     "traffic": _traffic("decode_tc_kernel/chunked_prefill", DECODE_TC_SOURCES),
+                     "traffic": _traffic("prefill_kernel/chunked_prefill", PREFILL_SOURCES),
                      "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
     del cp, out
     # QKV bias + YaRN rotary pass over the prefill's 8192 tokens (in place: the
