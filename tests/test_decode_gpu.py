@@ -138,3 +138,13 @@ def test_decode_full_batch128_long_auto_splits():
     seqs = sorted({int(lens.argmin()), int(lens.argmax()), 0, 64, 127})
     want, _ = oracle_decode(inp, seqs)
     assert_parity(out[seqs], want)
+
+
+@pytest.mark.slow
+def test_decode_131072_tokens():
+    # one query against 131072 cached tokens (8192 pages), chunks chosen per length
+    inp = workloads.make_decode([131072, 5], seed=13, sink_mode="normal2", num_splits=0, device="cuda")
+    out, lse = run(inp, with_lse=True)
+    want, want_lse = oracle_decode(inp)
+    assert_parity(out, want)
+    lse_close(lse, want_lse)

@@ -131,3 +131,19 @@ def test_prefill_full_ragged16():
     cpu = (inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu())
     want, _ = oracle.prefill_rows(*cpu, inp.scale, toks, heads)
     assert_parity(out[toks], want)
+
+
+@pytest.mark.slow
+def test_prefill_131072_tokens_sampled():
+    # the longest prompts the pages discuss (128000 tokens and beyond): one 131072-token
+    # sequence, rows near tile edges and the end, a few heads of different kv groups
+    L = 131072
+    inp = workloads.make_prefill([L], seed=12, sink_mode="normal2", device="cuda")
+    out, lse = run(inp, with_lse=True)
+    assert torch.isfinite(out).all()
+    toks = [0, 127, 128, 65535, 100000, L - 1]
+    heads = [0, 9, 63]
+    cpu = (inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu())
+    want, want_lse = oracle.prefill_rows(*cpu, inp.scale, toks, heads)
+    assert_parity(out[toks][:, heads], want)
+    lse_close(lse[toks][:, heads], want_lse)
