@@ -53,6 +53,11 @@ constexpr int kRows = 16;                       // MMA rows of one row tile
 // merge scratch per warp: m[16], d[16], o[16][64]
 constexpr int kScratchFloatsPerWarp = kRows * 2 + kRows * kD;
 static_assert(kConsumerWarps * kScratchFloatsPerWarp * 4 <= kRingBytes, "merge scratch aliases the ring");
+// Page i uses stage i % kStages and is consumed by warp i % kConsumerWarps: a
+// stage must always go to the same warp, or a warp could wait on a later phase
+// of a stage (by parity) before an earlier one completed, and arrive on the
+// stage's empty barrier out of turn.
+static_assert(kStages % kConsumerWarps == 0, "each ring stage must be consumed by one warp");
 
 __device__ __forceinline__ void chunk_range(const DecodeParams& p, int L, int s, int& n, int& pg0, int& pg1) {
   const int npages = (L + kPage - 1) / kPage;
