@@ -287,41 +287,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         n = max(1, (kend + kTile - 1) / kTile);  // at least one (possibly empty) tile: the unit still runs
         table_row = p.page_table + (size_t)seq_id[u.seq] * p.stride;
       }
-      // paged mode: this lane's page of the next tile, read one tile ahead so the
-      // page-table latency overlaps the current tile's copies
-      auto slabs = [&](int j) { return min(kTile / kPage, max(0, (kend - j * kTile + kPage - 1) / kPage)); };
-      int next_page = 0;
-      if constexpr (kPaged) next_page = lane < slabs(0) ? __ldg(table_row + lane) : 0;
-      for (int j = 0; j < n && ok; ++j) {
-        int np = 0, page = 0;  // paged mode: slabs of this tile, and this lane's page
-        if constexpr (kPaged) {
-          np = slabs(j);
-          page = next_page;
+      if constexpr (kPaged) {
+        // Per tile: both slots first, then its K and V slabs from 16 lanes in one go (lanes
+        // 0..7 K, 8..15 V).  Copies issued lane-parallel: from one lane the copy issue alone
+        // paced the kernel.  Page ids are read one tile ahead (lanes 0..7).
+        auto slabs = [&](int j) { return min(kTile / kPage, max(0, (kend - j * kTile + kPage - 1) / kPage)); };
+        int next_page = lane < slabs(0) ? __ldg(table_row + lane) : 0;
+        for (int j = 0; j < n && ok; ++j) {
+          const int np = slabs(j), page = next_page;
           if (j + 1 < n && lane < slabs(j + 1)) next_page = __ldg(table_row + (j + 1) * (kTile / kPage) + lane);
-        }
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t slot = ring_i % kSlots;
+          const uint32_t ks = ring_i % kSlots, vs = (ring_i + 1) % kSlots;
           if (ring_i >= kSlots &&
               !(ok = __all_sync(0xffffffffu,
-                                wait_or_abort(bars.slot_empty + slot, ((ring_i / kSlots) - 1) & 1, p, abort_flag))))
+                                wait_or_abort(bars.slot_empty + ks, ((ring_i / kSlots) - 1) & 1, p, abort_flag))))
             break;
-          if constexpr (kPaged) {
-            if (!p.withhold_copies) {
-              if (elect_one()) mbar_arrive_expect_tx(bars.slot_full + slot, np * kSlabBytes);
-              __syncwarp();
-              if (lane < np)
-                tma_load_2d(ring + slot * kTileBytes + lane * kSlabBytes, kv ? &vmap : &kmap, bars.slot_full + slot,
-                            0, (page * p.hkv + u.g) * kPage);
+          if (ring_i + 1 >= kSlots &&
+              !(ok = __all_sync(0xffffffffu, wait_or_abort(bars.slot_empty + vs, (((ring_i + 1) / kSlots) - 1) & 1,
+                                                           p, abort_flag))))
+            break;
+          if (!p.withhold_copies) {
+            if (elect_one()) {
+              mbar_arrive_expect_tx(bars.slot_full + ks, np * kSlabBytes);
+              mbar_arrive_expect_tx(bars.slot_full + vs, np * kSlabBytes);
             }
-          } else {
+            __syncwarp();
+            const int sl = lane & 7;
+            const bool is_v = lane >= 8;
+            const int pg = __shfl_sync(0xffffffffu, page, sl);
+            const uint32_t slot = is_v ? vs : ks;
+            if (lane < 16 && sl < np)
+              tma_load_2d(ring + slot * kTileBytes + sl * kSlabBytes, is_v ? &vmap : &kmap, bars.slot_full + slot, 0,
+                          (pg * p.hkv + u.g) * kPage);
+          }
+          ring_i += 2;
+        }
+      } else {
+        for (int j = 0; j < n && ok; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t slot = ring_i % kSlots;
+            if (ring_i >= kSlots &&
+                !(ok = __all_sync(0xffffffffu,
+                                  wait_or_abort(bars.slot_empty + slot, ((ring_i / kSlots) - 1) & 1, p, abort_flag))))
+              break;
             if (!p.withhold_copies && elect_one()) {
               mbar_arrive_expect_tx(bars.slot_full + slot, kTileBytes);
               tma_load_3d(ring + slot * kTileBytes, kv ? &vmap : &kmap, bars.slot_full + slot, 0, u.g,
                           kv0 + j * kTile);
             }
+            ++ring_i;
           }
-          ++ring_i;
         }
       }
     }
