@@ -126,12 +126,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -168,17 +162,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-// Per-warp register budget changes (all four warps of a warpgroup execute the
-// same one).  The sum over the block must not exceed the launch allocation.
-template <uint32_t N>
-__device__ __forceinline__ void regs_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // acc.x += low bf16 half of pk, acc.y += high half (each widened exactly to

@@ -1,5 +1,6 @@
 // Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05) and the
-// tensor memory (TMEM) of sm_100-family GPUs, as used by the prefill kernel.
+// tensor memory (TMEM) of sm_100-family GPUs, as used by the prefill and the
+// tensor-core decode kernels.
 //
 // Encodings follow the PTX ISA descriptions of tcgen05:
 //   * shared-memory matrix descriptor (64 bit): start address >> 4 in bits
@@ -84,32 +85,17 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // ------------------------------------------------------------ TMEM <-> registers
 // 32x32b shape: thread i of the warp reads/writes TMEM lane (lane base + i),
 // N consecutive 32-bit columns starting at the address's column.
-#define SA_REG8(p) "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3]), "=r"(p[4]), "=r"(p[5]), "=r"(p[6]), "=r"(p[7])
 #define SA_REG8_OFF(p, o)                                                                                     \
   "=r"(p[o + 0]), "=r"(p[o + 1]), "=r"(p[o + 2]), "=r"(p[o + 3]), "=r"(p[o + 4]), "=r"(p[o + 5]), "=r"(p[o + 6]), \
       "=r"(p[o + 7])
 #define SA_IN8_OFF(p, o) \
   "r"(p[o + 0]), "r"(p[o + 1]), "r"(p[o + 2]), "r"(p[o + 3]), "r"(p[o + 4]), "r"(p[o + 5]), "r"(p[o + 6]), "r"(p[o + 7])
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : SA_REG8_OFF(r, 0), SA_REG8_OFF(r, 8), SA_REG8_OFF(r, 16), SA_REG8_OFF(r, 24)
-      : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : SA_REG8_OFF(r, 0), SA_REG8_OFF(r, 8)
       : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      SA_IN8_OFF(r, 0), SA_IN8_OFF(r, 8), SA_IN8_OFF(r, 16), SA_IN8_OFF(r, 24)
-      : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
