@@ -269,3 +269,22 @@ def test_qkv_rope_rejects_bad_arguments_on_host(lib, kw, status):
 
 def test_qkv_rope_empty_is_noop(lib):
     assert _rope_call(lib, T=0, q=None) == 0
+
+
+def _declared_arities():
+    """Parameter count of every function the header declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(sink_attn_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    # a ctypes signature with a missing or extra argument would silently shift every later one
+    arities = _declared_arities()
+    assert set(arities) == set(binding.EXPORTS), set(arities) ^ set(binding.EXPORTS)
+    for name, (_, args) in binding.EXPORTS.items():
+        assert len(args) == arities[name], f"{name}: binding has {len(args)} arguments, header {arities[name]}"
