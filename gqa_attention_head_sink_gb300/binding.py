@@ -124,8 +124,9 @@ def sink_attn_get_device_error(stream=None) -> int:
 def sink_attn_prefill(q, k, v, sinks, cu_seqlens, scale: float, out=None, out_dtype=torch.float32,
                       lse=None, max_seqlen: Optional[int] = None, stream=None):
     """Causal varlen prefill.  q [T,Hq,64], k/v [T,Hkv,64] bf16; sinks [Hq] fp32;
-    cu_seqlens [B+1] int32.  Returns out [T,Hq,64] (bf16 or fp32).  Pass
-    ``max_seqlen`` to avoid a device->host read of the lengths."""
+    cu_seqlens [B+1] int32.  Returns out [T,Hq,64] (bf16 or fp32).
+    ``max_seqlen`` (host upper bound on the lengths) defaults to T, which
+    needs no read of the device, so the call can be captured in a CUDA graph."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
@@ -138,8 +139,8 @@ def sink_attn_prefill(q, k, v, sinks, cu_seqlens, scale: float, out=None, out_dt
     if sinks.shape[0] != hq:
         raise ValueError("sinks must have one entry per query head")
     B = cu_seqlens.shape[0] - 1
-    if max_seqlen is None:
-        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 0
+    if max_seqlen is None:  # an upper bound known without reading the device (graph-capturable)
+        max_seqlen = T
     if out is None:
         out = torch.empty((T, hq, d), dtype=out_dtype, device=q.device)
     if out.dtype not in (torch.bfloat16, torch.float32):
@@ -186,7 +187,10 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
     [num_pages,Hkv,16,64] bf16; page_table [B,stride] int32; seqlens [B]
     int32; sinks [Hq] fp32.  ``workspace``: optional uint8 CUDA tensor of at
     least sink_attn_decode_workspace_bytes(...) bytes (else the library
-    allocates in stream order).  Returns out [B,Hq,64]."""
+    allocates in stream order).  ``max_seqlen`` (host upper bound on the
+    lengths, fixes the grid) defaults to stride * page_size, which needs no
+    read of the device (graph-capturable); the true maximum sizes the work
+    exactly.  Returns out [B,Hq,64]."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_pages, "k_pages", torch.bfloat16, 4)
     _need(v_pages, "v_pages", torch.bfloat16, 4)
@@ -199,8 +203,8 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
         raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
     if page_table.shape[0] != B or seqlens.shape[0] != B:
         raise ValueError("page_table and seqlens need one row per sequence")
-    if max_seqlen is None:
-        max_seqlen = int(seqlens.max().item()) if B > 0 else 0
+    if max_seqlen is None:  # the page-table width bounds every length: no device read
+        max_seqlen = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
     _need(out, "out", out.dtype, 3)
@@ -238,8 +242,8 @@ def sink_attn_decode_multi(q, k_pages, v_pages, page_table, seqlens, sinks, scal
         raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
     if page_table.shape[0] != B or seqlens.shape[0] != B:
         raise ValueError("page_table and seqlens need one row per sequence")
-    if max_seqlen is None:
-        max_seqlen = int(seqlens.max().item()) if B > 0 else 0
+    if max_seqlen is None:  # the page-table width bounds every length: no device read
+        max_seqlen = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((B, n, hq, d), dtype=out_dtype, device=q.device)
     _need(out, "out", out.dtype, 4)
@@ -290,10 +294,12 @@ def sink_attn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqle
         raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
     if page_table.shape[0] != B or cu_seqlens_q.shape[0] != B + 1:
         raise ValueError("page_table needs one row and cu_seqlens_q one offset per sequence (plus one)")
+    # upper bounds known without reading the device (graph-capturable); pass the true
+    # maxima to size the work exactly
     if max_seqlen_q is None:
-        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B > 0 else 0
+        max_seqlen_q = total_q
     if max_seqlen_k is None:
-        max_seqlen_k = int(seqlens_k.max().item()) if B > 0 else 0
+        max_seqlen_k = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((total_q, hq, d), dtype=out_dtype, device=q.device)
     _need(out, "out", out.dtype, 3)
@@ -378,8 +384,8 @@ def sink_attn_decode_noalloc(q, k_pages, v_pages, page_table, seqlens, sinks, sc
     _need(sinks, "sinks", torch.float32, 1)
     B, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_pages.shape
-    if max_seqlen is None:
-        max_seqlen = int(seqlens.max().item()) if B > 0 else 0
+    if max_seqlen is None:  # the page-table width bounds every length: no device read
+        max_seqlen = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
     _need(out, "out", out.dtype, 3)

@@ -74,3 +74,38 @@ def test_prefill_graph_replay_follows_new_data():
                                 max_seqlen=p.max_seqlen)
     torch.cuda.synchronize()
     assert torch.equal(out, want)
+
+
+def test_capture_with_default_bounds_needs_no_device_read():
+    # without max_seqlen the bindings use bounds known on the host (page-table width, token
+    # count): nothing reads the device, so capture works and replays follow new inputs
+    d = workloads.make_decode([700, 1500], seed=43, sink_mode="normal2", num_splits=0, q_len=4, device="cuda")
+    bound = d.page_table.shape[1] * 16
+    need = sa.sink_attn_decode_multi_workspace_bytes(d.batch, 4, bound, 64, 8, 64, 16, 0)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    out = torch.empty(d.q.shape, dtype=torch.float32, device="cuda")
+    c = workloads.make_paged_prefill([900, 300], [300, 300], seed=44, sink_mode="mixed", device="cuda")
+    out_c = torch.empty(c.q.shape, dtype=torch.float32, device="cuda")
+
+    def step():
+        sa.sink_attn_decode_multi(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale,
+                                  out=out, workspace=ws)
+        sa.sink_attn_prefill_paged(c.q, c.k_pages, c.v_pages, c.page_table, c.cu_seqlens_q, c.seqlens_t, c.sinks,
+                                   c.scale, out=out_c)
+
+    step()  # one-time set-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    g = torch.Generator(device="cuda").manual_seed(9)
+    d.q.copy_(torch.randn(d.q.shape, generator=g, device="cuda").to(torch.bfloat16))
+    c.q.copy_(torch.randn(c.q.shape, generator=g, device="cuda").to(torch.bfloat16))
+    graph.replay()
+    torch.cuda.synchronize()
+    want = sa.sink_attn_decode_multi(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale,
+                                     workspace=ws)
+    want_c = sa.sink_attn_prefill_paged(c.q, c.k_pages, c.v_pages, c.page_table, c.cu_seqlens_q, c.seqlens_t,
+                                        c.sinks, c.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want) and torch.equal(out_c, want_c)
