@@ -38,6 +38,8 @@ constexpr int kHalf = kD / 2;
 constexpr int kThreads = 256;
 constexpr int kTokensPerBlock = 8;
 constexpr int kLanesPerRow = 4;  // a lane rotates 8 planes: 16 bytes of each half
+// the table phase gives each thread exactly one (token, plane) entry
+static_assert(kThreads == kTokensPerBlock * kHalf, "one cos/sin entry per thread");
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
