@@ -151,3 +151,14 @@ def test_decode_multi_full_size_sampled(q_len):
     assert_parity(out[seqs], want, bf16_output=True)
     lse_close(lse[seqs], want_lse)
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("q_len", [2, 8])  # the split kernel, then the tensor-core kernel
+def test_decode_multi_large_logits(q_len):
+    # softmax scale 1: logits ~8x larger, the running maximum moves often and far
+    inp = workloads.make_decode([3000, 129, 7], seed=37, sink_mode="mixed", q_len=q_len, num_splits=0,
+                                scale=1.0, device="cuda")
+    out, lse = run(inp, with_lse=True)
+    want, want_lse = oracle_multi(inp)
+    assert_parity(out, want)
+    lse_close(lse, want_lse)

@@ -147,3 +147,29 @@ def test_prefill_131072_tokens_sampled():
     want, want_lse = oracle.prefill_rows(*cpu, inp.scale, toks, heads)
     assert_parity(out[toks][:, heads], want)
     lse_close(lse[toks][:, heads], want_lse)
+
+
+@pytest.mark.parametrize("how", ["growing_keys", "scale_1"])
+def test_prefill_running_max_moves_often(how):
+    # the running maximum is raised only when a tile beats it by more than 8 (log2 units), and
+    # O is rescaled then: keys whose norm grows along the sequence raise it at nearly every key
+    # tile; a softmax scale of 1 (logits ~8x larger) raises it often and by a lot
+    lens = [1000, 700]
+    inp = workloads.make_prefill(lens, num_q_heads=16, num_kv_heads=2, seed=14, sink_mode="mixed", device="cuda")
+    scale = inp.scale
+    if how == "growing_keys":
+        start = 0
+        for L in lens:
+            grow = (1.0 + torch.arange(L, device="cuda", dtype=torch.float32) / 60.0)[:, None, None]
+            inp.k[start:start + L] = (inp.k[start:start + L].float() * grow).to(torch.bfloat16)
+            start += L
+    else:
+        scale = 1.0
+    lse = torch.empty((inp.total_tokens, inp.num_q_heads), dtype=torch.float32, device="cuda")
+    out = sa.sink_attn_prefill(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, scale, lse=lse,
+                               max_seqlen=inp.max_seqlen)
+    torch.cuda.synchronize()
+    want, want_lse = oracle.prefill(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu(),
+                                    scale)
+    assert_parity(out, want)
+    lse_close(lse, want_lse)

@@ -126,3 +126,19 @@ def test_prefill_paged_full_size_sampled():
                                        torch.tensor([L - n + t + 1], dtype=torch.int32), inp.sinks.cpu(), inp.scale)
         assert_parity(out[t][None], want, bf16_output=True)
         lse_close(lse[t][None], want_lse)
+
+
+@pytest.mark.parametrize("n_new", [700, 90])  # the prefill kernel's paged mode, then the tensor-core decode kernel
+def test_prefill_paged_running_max_moves_often(n_new):
+    # keys whose norm grows along the cache raise the running maximum at nearly every key tile
+    L = 1500
+    inp = workloads.make_paged_prefill([L], [n_new], num_q_heads=16, num_kv_heads=2, seed=55, sink_mode="mixed",
+                                       device="cuda")
+    j = torch.arange(L, device="cuda")
+    grow = (1.0 + j.float() / 80.0)[:, None]
+    pages = inp.page_table[0, j // 16].long()
+    inp.k_pages[pages, :, j % 16] = (inp.k_pages[pages, :, j % 16].float() * grow[:, None, :]).to(torch.bfloat16)
+    out, lse = run(inp, with_lse=True)
+    want, want_lse = oracle_paged(inp)
+    assert_parity(out, want)
+    lse_close(lse, want_lse)
