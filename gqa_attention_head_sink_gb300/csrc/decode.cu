@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
   const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
   int n, pg0, pg1;
   chunk_range(p, L, s, n, pg0, pg1);
+  // the merge kernel may be scheduled once every CTA of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (s >= n) return;
   const int count = max(0, pg1 - pg0);
 
@@ -368,8 +370,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const __grid_
 
 // Combine the chunks' partial states: one warp per (row of q, query head).
 // Lane l owns output dims 2l, 2l+1.  Chunk c contributes with weight
-// 2^(m_c - M), M = max_c m_c; chunks that saw nothing have m_c = -inf.
+// 2^(m_c - M), M = max_c m_c; chunks that saw nothing have m_c = -inf (and
+// d_c = 0, o_c = 0), hence weight 0.  Launched as a programmatic dependent of
+// the chunk kernel: it waits for that grid's results before reading them.
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (wid >= p.total_q * p.hq) return;
   const int row = wid / p.hq;
@@ -389,22 +394,40 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
   int n, pg0, pg1;
   chunk_range(p, L, 0, n, pg0, pg1);
   const size_t slot0 = (size_t)wid * p.max_splits;
-  const float* md = p.ws_md + slot0 * 2;
+  const float2* md = reinterpret_cast<const float2*>(p.ws_md) + slot0;  // (m_c, d_c)
   float M = -INFINITY;
-  for (int c = lane; c < n; c += 32) M = fmaxf(M, md[2 * c]);
+  for (int c = lane; c < n; c += 32) M = fmaxf(M, md[c].x);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float W = 0.f, a0 = 0.f, a1 = 0.f;
   if (M != -INFINITY) {
-    for (int c = 0; c < n; ++c) {
-      const float mc = md[2 * c];
-      if (mc == -INFINITY) continue;
-      const float f = fast_exp2(mc - M);
-      W += md[2 * c + 1] * f;
-      const float2 oc = *reinterpret_cast<const float2*>(p.ws_o + (slot0 + c) * kD + 2 * lane);
-      a0 += oc.x * f;
-      a1 += oc.y * f;
+    const float2* o = reinterpret_cast<const float2*>(p.ws_o + slot0 * kD) + lane;  // chunk c at o[c * 32]
+    for (int base = 0; base < n; base += 32) {
+      // chunk base + lane's weight on this lane; the dims loop reads it by shuffle
+      float f = 0.f;
+      if (base + lane < n) {
+        const float2 v = md[base + lane];
+        f = fast_exp2(v.x - M);  // 0 for a chunk that saw nothing
+        W += v.y * f;
+      }
+      const int cnt = min(32, n - base);
+      for (int k = 0; k < cnt; k += 8) {  // eight chunks' loads in flight before their adds
+        float2 oc[8];
+        float fk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          fk[u] = __shfl_sync(0xffffffffu, f, k + u);
+          oc[u] = k + u < cnt ? o[(size_t)(base + k + u) * 32] : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          a0 += oc[u].x * fk[u];
+          a1 += oc[u].y * fk[u];
+        }
+      }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   const size_t o_off = (size_t)wid * kD + 2 * lane;
@@ -414,6 +437,21 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o_off) = pack_bf16x2(a0 * inv, a1 * inv);
   }
   if (p.lse && lane == 0) p.lse[wid] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+}
+
+cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream) {
+  const long long warps = (long long)p.total_q * p.hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel, p);
 }
 
 size_t decode_smem_bytes() { return kRingBytes + 2 * kStages * 8 + 16 + 1024; }
@@ -437,9 +475,7 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   decode_split_kernel<<<grid, kThreads, decode_smem_bytes(), stream>>>(kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.direct) return e;
-  const long long warps = (long long)p.total_q * p.hq;
-  decode_merge_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_decode_merge(p, stream);
 }
 
 }  // namespace sa

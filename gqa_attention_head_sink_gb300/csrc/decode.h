@@ -63,6 +63,10 @@ size_t decode_smem_bytes();
 cudaError_t decode_configure();
 int decode_threads();
 
+// Enqueue the merge kernel as a programmatic dependent launch of the chunk
+// kernel just enqueued on the same stream.
+cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream);
+
 // Enqueue the chunk kernel and, when chunks are merged, the merge kernel.
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                           cudaStream_t stream);

@@ -83,6 +83,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 __global__ void __launch_bounds__(kThreads, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  // the merge kernel may be scheduled once every CTA of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int s = blockIdx.x, g = blockIdx.y;
   // blockIdx.z = r * batch + b with tile = row_tiles - 1 - r: the last tiles of
   // every sequence (which see the most keys) are launched first
@@ -409,9 +411,7 @@ cudaError_t launch_decode_tc(const CUtensorMap& qmap, const CUtensorMap& kmap, c
   decode_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.direct) return e;
-  const long long warps = (long long)p.total_q * p.hq;
-  decode_merge_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_decode_merge(p, stream);
 }
 
 }  // namespace sa
