@@ -403,53 +403,108 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
 
 def _e2e(sa, pre, dec, dev, stream, args):
     """Prefill and decode through the public API from pinned host buffers:
-    each step copies its inputs host->device, runs, and reads the outputs back."""
-    steps = max(3, min(args.steps, 20))
+    every step copies its inputs host->device, runs, and reads its output
+    back.  Serial: one stream, each step's copies and call back to back.
+    Pipelined (the reported value): a double-buffered serving loop, step i's
+    input copy on a copy-in stream overlapping step i-1's call and step i-2's
+    read-back on a copy-out stream; events order each buffer's reuse."""
+    steps = max(4, min(args.steps, 20))
     h = {n: getattr(pre, n).cpu().pin_memory() for n in ("q", "k", "v", "sinks", "cu_seqlens")}
     hd = {n: getattr(dec, n).cpu().pin_memory() for n in ("q", "k_pages", "v_pages", "page_table", "seqlens_t",
                                                            "sinks")}
-    d = {n: torch.empty_like(t, device=dev) for n, t in h.items()}
-    dd = {n: torch.empty_like(t, device=dev) for n, t in hd.items()}
-    out_p = torch.empty(pre.q.shape, dtype=torch.bfloat16, device=dev)
-    out_d = torch.empty(dec.q.shape, dtype=torch.bfloat16, device=dev)
-    host_p = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
-    host_d = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    d = [{n: torch.empty_like(t, device=dev) for n, t in h.items()} for _ in range(2)]
+    dd = [{n: torch.empty_like(t, device=dev) for n, t in hd.items()} for _ in range(2)]
+    out_p = [torch.empty(pre.q.shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    out_d = [torch.empty(dec.q.shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    host_p = [torch.empty(out_p[0].shape, dtype=out_p[0].dtype).pin_memory() for _ in range(2)]
+    host_d = [torch.empty(out_d[0].shape, dtype=out_d[0].dtype).pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def step_prefill():
-        for n in h:
-            d[n].copy_(h[n], non_blocking=True)
-        sa.sink_attn_prefill(d["q"], d["k"], d["v"], d["sinks"], d["cu_seqlens"], pre.scale, out=out_p,
-                             max_seqlen=pre.max_seqlen)
-        host_p.copy_(out_p, non_blocking=True)
+    def call_prefill(b):
+        sa.sink_attn_prefill(d[b]["q"], d[b]["k"], d[b]["v"], d[b]["sinks"], d[b]["cu_seqlens"], pre.scale,
+                             out=out_p[b], max_seqlen=pre.max_seqlen)
 
-    def step_decode():
-        for n in hd:
-            dd[n].copy_(hd[n], non_blocking=True)
-        sa.sink_attn_decode(dd["q"], dd["k_pages"], dd["v_pages"], dd["page_table"], dd["seqlens_t"], dd["sinks"],
-                            dec.scale, num_splits=dec.num_splits, out=out_d, max_seqlen=dec.max_seqlen)
-        host_d.copy_(out_d, non_blocking=True)
+    def call_decode(b):
+        x = dd[b]
+        sa.sink_attn_decode(x["q"], x["k_pages"], x["v_pages"], x["page_table"], x["seqlens_t"], x["sinks"],
+                            dec.scale, num_splits=dec.num_splits, out=out_d[b], max_seqlen=dec.max_seqlen)
 
-    res = {}
-    for name, fn in (("prefill", step_prefill), ("decode", step_decode)):
-        fn()
+    def serial(src, dst, call, out, host):
+        def step(i):
+            for n in src:
+                dst[0][n].copy_(src[n], non_blocking=True)
+            call(0)
+            host[0].copy_(out[0], non_blocking=True)
+        return step
+
+    def timed_serial(step):
+        with torch.cuda.stream(stream):
+            step(0)
+            torch.cuda.synchronize()
+            a, b = _events()
+            a.record(stream)
+            for i in range(steps):
+                step(i)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    def timed_pipelined(src, dst, call, out, host):
+        in_done = [torch.cuda.Event() for _ in range(2)]
+        run_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+
+        def run(n_steps, first, last):
+            for i in range(n_steps):
+                b = i % 2
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(run_done[b])  # the call of step i-2 has read buffer b
+                    if i == 0 and first is not None:
+                        first.record(s_in)
+                    for n in src:
+                        dst[b][n].copy_(src[n], non_blocking=True)
+                    in_done[b].record(s_in)
+                with torch.cuda.stream(stream):
+                    stream.wait_event(in_done[b])
+                    if i >= 2:
+                        stream.wait_event(out_done[b])  # step i-2's output has been read back
+                    call(b)
+                    run_done[b].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(run_done[b])
+                    host[b].copy_(out[b], non_blocking=True)
+                    out_done[b].record(s_out)
+                    if i == n_steps - 1 and last is not None:
+                        last.record(s_out)
+
+        run(2, None, None)
         torch.cuda.synchronize()
         a, b = _events()
-        a.record(stream)
-        for _ in range(steps):
-            fn()
-        b.record(stream)
+        run(steps, a, b)
         torch.cuda.synchronize()
-        res[name] = a.elapsed_time(b) / steps
+        return a.elapsed_time(b) / steps
+
+    res = {}
+    res["prefill_serial"] = timed_serial(serial(h, d, call_prefill, out_p, host_p))
+    res["prefill"] = timed_pipelined(h, d, call_prefill, out_p, host_p)
+    res["decode_serial"] = timed_serial(serial(hd, dd, call_decode, out_d, host_d))
+    res["decode"] = timed_pipelined(hd, dd, call_decode, out_d, host_d)
     flops = workloads.prefill_flops(pre.seqlens, pre.num_q_heads)
     dbytes = workloads.decode_bytes(dec.seqlens, dec.num_q_heads, dec.num_kv_heads, out_bytes=2)
     h2d_p = sum(t.numel() * t.element_size() for t in h.values())
     h2d_d = sum(t.numel() * t.element_size() for t in hd.values())
     return {"value": round(flops / (res["prefill"] * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d_p, "d2h_bytes_per_step": host_p.numel() * 2,
+            "h2d_bytes_per_step": h2d_p, "d2h_bytes_per_step": host_p[0].numel() * 2,
             "ms_per_step": round(res["prefill"], 4),
+            "loop": "pipelined: double-buffered, input copy / call / read-back on three streams",
+            "serial": {"value": round(flops / (res["prefill_serial"] * 1e-3) / 1e12, 3),
+                       "ms_per_step": round(res["prefill_serial"], 4)},
             "decode": {"value": round(dbytes / (res["decode"] * 1e-3) / 1e9, 2), "unit": "GB/s",
-                       "h2d_bytes_per_step": h2d_d, "d2h_bytes_per_step": host_d.numel() * 2,
-                       "ms_per_step": round(res["decode"], 4)},
+                       "h2d_bytes_per_step": h2d_d, "d2h_bytes_per_step": host_d[0].numel() * 2,
+                       "ms_per_step": round(res["decode"], 4),
+                       "serial": {"value": round(dbytes / (res["decode_serial"] * 1e-3) / 1e9, 2),
+                                  "ms_per_step": round(res["decode_serial"], 4)}},
             "steps": steps}
 
 
