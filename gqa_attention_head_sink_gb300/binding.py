@@ -95,6 +95,18 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _workspace(n: int, device, stream):
+    """A workspace of n bytes from PyTorch's caching allocator, tied to the
+    stream the call runs on (None when the call needs none, or when n is the
+    size query's error value: the call itself then reports the arguments)."""
+    if n == 0 or n == ctypes.c_size_t(-1).value:
+        return None
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    if stream is not None:
+        ws.record_stream(stream)
+    return ws
+
+
 def _need(t: torch.Tensor, name: str, dtype, ndim: int):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -186,8 +198,8 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
     """Split-KV paged decode.  q [B,Hq,64] bf16; k_pages/v_pages
     [num_pages,Hkv,16,64] bf16; page_table [B,stride] int32; seqlens [B]
     int32; sinks [Hq] fp32.  ``workspace``: optional uint8 CUDA tensor of at
-    least sink_attn_decode_workspace_bytes(...) bytes (else the library
-    allocates in stream order).  ``max_seqlen`` (host upper bound on the
+    least sink_attn_decode_workspace_bytes(...) bytes (else one comes from
+    PyTorch's caching allocator for this call).  ``max_seqlen`` (host upper bound on the
     lengths, fixes the grid) defaults to stride * page_size, which needs no
     read of the device (graph-capturable); the true maximum sizes the work
     exactly.  Returns out [B,Hq,64]."""
@@ -210,6 +222,9 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
     _need(out, "out", out.dtype, 3)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        workspace = _workspace(load().sink_attn_decode_workspace_bytes(B, int(max_seqlen), hq, hkv, d, page_size,
+                                                                       int(num_splits)), q.device, stream)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
@@ -249,6 +264,10 @@ def sink_attn_decode_multi(q, k_pages, v_pages, page_table, seqlens, sinks, scal
     _need(out, "out", out.dtype, 4)
     if lse is not None:
         _need(lse, "lse", torch.float32, 3)
+    if workspace is None:
+        workspace = _workspace(load().sink_attn_decode_multi_workspace_bytes(B, n, int(max_seqlen), hq, hkv, d,
+                                                                             page_size, int(num_splits)),
+                               q.device, stream)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
@@ -305,6 +324,11 @@ def sink_attn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqle
     _need(out, "out", out.dtype, 3)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        workspace = _workspace(load().sink_attn_prefill_paged_workspace_bytes(B, total_q, int(max_seqlen_q),
+                                                                              int(max_seqlen_k), hq, hkv, d,
+                                                                              page_size, int(num_splits)),
+                               q.device, stream)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()

@@ -6,6 +6,8 @@ the launch the benchmark times, and batch 128 x 16K-32K tokens with chunks
 chosen per length) are compared on sampled sequences (every head, every
 dimension), which the oracle evaluates one by one.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -102,12 +104,22 @@ def test_decode_is_deterministic_and_ignores_page_placement():
 
 
 def test_decode_caller_workspace_matches_library_workspace():
+    # caller workspace, the binding's default (PyTorch's caching allocator) and the C ABI's own
+    # stream-ordered allocation (null workspace) give the same bits
     inp = workloads.make_decode([2000, 3000], seed=13, num_splits=6, device="cuda")
     need = sa.sink_attn_decode_workspace_bytes(inp.batch, inp.max_seqlen, 64, 8, 64, 16, 6)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     a, _ = run(inp, workspace=ws)
     b, _ = run(inp)
-    assert torch.equal(a, b)
+    c = torch.empty_like(a)
+    st = sa.load().sink_attn_decode(inp.q.data_ptr(), inp.k_pages.data_ptr(), inp.v_pages.data_ptr(),
+                                    inp.page_table.data_ptr(), inp.page_table.shape[1], inp.seqlens_t.data_ptr(),
+                                    inp.batch, inp.max_seqlen, inp.k_pages.shape[0], inp.sinks.data_ptr(), 64, 8,
+                                    64, 16, inp.scale, 6, c.data_ptr(), 1, None, None, 0,
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
 
 
 def test_decode_rejects_bad_shapes():
