@@ -45,7 +45,49 @@ bool g_prefill_attr_set[kMaxDevices] = {};
 bool g_decode_attr_set[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+cudaMemPool_t g_ws_pool[kMaxDevices] = {};
+bool g_ws_pool_failed[kMaxDevices] = {};
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace for a call that passes none, in stream order on `s`.  Outside
+// stream capture it comes from a library-owned pool per device whose freed
+// memory stays reserved for later calls (release threshold: unlimited), so a
+// call after a synchronize does not go back to the driver; during capture (or
+// if the pool cannot be made) from cudaMallocAsync, which capture records as a
+// graph allocation node.
+cudaError_t workspace_alloc(void** ws, size_t bytes, cudaStream_t s) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return e;
+  int dev = -1;
+  if (cap == cudaStreamCaptureStatusNone && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+    cudaMemPool_t pool = nullptr;
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      if (!g_ws_pool[dev] && !g_ws_pool_failed[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        uint64_t keep = UINT64_MAX;
+        if (cudaMemPoolCreate(&p, &props) == cudaSuccess &&
+            cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep) == cudaSuccess) {
+          g_ws_pool[dev] = p;
+        } else {
+          if (p) cudaMemPoolDestroy(p);
+          cudaGetLastError();
+          g_ws_pool_failed[dev] = true;
+        }
+      }
+      pool = g_ws_pool[dev];
+    }
+    if (pool) return cudaMallocFromPoolAsync(ws, bytes, pool, s);
+  }
+  return cudaMallocAsync(ws, bytes, s);
+}
 
 uint64_t wait_limit_ns() {
   static uint64_t v = [] {
@@ -400,7 +442,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   void* ws = workspace;
   bool owned = false;
   if (pl.ws_bytes && !ws) {
-    if (cudaMallocAsync(&ws, pl.ws_bytes, s) != cudaSuccess) {
+    if (workspace_alloc(&ws, pl.ws_bytes, s) != cudaSuccess) {
       cudaGetLastError();
       return SINK_ATTN_ERR_NO_MEMORY;
     }

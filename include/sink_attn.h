@@ -118,7 +118,11 @@ int sink_attn_prefill(const void* q, const void* k, const void* v, const float* 
  *   workspace   device scratch for the per-chunk partial states, at least
  *               sink_attn_decode_workspace_bytes(...) bytes, 256-byte
  *               aligned.  NULL: the library allocates and frees it in stream
- *               order (cudaMallocAsync / cudaFreeAsync) when it is needed.
+ *               order when it is needed: from a library-owned memory pool
+ *               per device (cudaMallocFromPoolAsync / cudaFreeAsync), which
+ *               keeps freed memory for later calls (up to the largest
+ *               workspace used) until the process exits; during stream
+ *               capture with cudaMallocAsync (a graph allocation node).
  * batch == 0 is a no-op returning SINK_ATTN_OK.
  */
 int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages,
