@@ -122,6 +122,24 @@ def test_decode_caller_workspace_matches_library_workspace():
     assert torch.equal(a, b) and torch.equal(a, c)
 
 
+def test_decode_default_workspace_on_another_stream():
+    # the binding's default workspace is tied to the stream the call runs on: allocations made on
+    # the current stream right after the call must not reuse it while that stream still works
+    inp = workloads.make_decode([3000, 5000, 4000], seed=14, num_splits=5, device="cuda")
+    want, _ = run(inp)
+    need = sa.sink_attn_decode_workspace_bytes(inp.batch, inp.max_seqlen, 64, 8, 64, 16, 5)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    out = torch.empty_like(want)
+    for _ in range(3):
+        sa.sink_attn_decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.seqlens_t, inp.sinks, inp.scale,
+                            num_splits=5, out=out, max_seqlen=inp.max_seqlen, stream=side)
+        junk = [torch.full((need // 4 + 1,), float("nan"), device="cuda") for _ in range(8)]
+        del junk
+    torch.cuda.synchronize()
+    assert torch.equal(out, want)
+
+
 def test_decode_rejects_bad_shapes():
     inp = workloads.make_decode([20], seed=1, device="cuda")
     with pytest.raises(sa.SinkAttnError) as e:

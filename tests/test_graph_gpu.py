@@ -109,3 +109,41 @@ def test_capture_with_default_bounds_needs_no_device_read():
                                         c.sinks, c.scale)
     torch.cuda.synchronize()
     assert torch.equal(out, want) and torch.equal(out_c, want_c)
+
+
+def test_capture_with_default_workspaces():
+    # neither a caller workspace from the binding (PyTorch's graph pool serves it) nor one
+    # through the C ABI (a null pointer: the library records a graph allocation node)
+    import ctypes
+
+    bound = 2048
+    d = workloads.make_decode([bound, 700], seed=44, sink_mode="normal2", num_splits=4, device="cuda")
+    out_a = torch.empty((d.batch, 64, 64), dtype=torch.float32, device="cuda")
+    out_b = torch.empty_like(out_a)
+    lib = sa.load()
+
+    def step():
+        sa.sink_attn_decode(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale, num_splits=4,
+                            out=out_a, max_seqlen=bound)
+        st = lib.sink_attn_decode(d.q.data_ptr(), d.k_pages.data_ptr(), d.v_pages.data_ptr(), d.page_table.data_ptr(),
+                                  d.page_table.shape[1], d.seqlens_t.data_ptr(), d.batch, bound, d.k_pages.shape[0],
+                                  d.sinks.data_ptr(), 64, 8, 64, 16, d.scale, 4, out_b.data_ptr(), 1, None, None, 0,
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0, st
+
+    step()  # one-time set-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    g = torch.Generator(device="cuda").manual_seed(9)
+    d.q.copy_(torch.randn(d.q.shape, generator=g, device="cuda").to(torch.bfloat16))
+    d.seqlens_t.copy_(torch.tensor([1500, 2048], dtype=torch.int32, device="cuda"))
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    want = sa.sink_attn_decode(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale, num_splits=4,
+                               max_seqlen=bound)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, want) and torch.equal(out_b, want)
+    assert sa.sink_attn_get_device_error() == 0
