@@ -428,15 +428,16 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
       g_decode_attr_set[dev] = true;
     }
   }
-  const uint64_t rows = (uint64_t)num_pages * num_kv_heads * kPageSize;
-  CUtensorMap kmap, vmap;
-  if ((st = encode_rows64(&kmap, k_pages, rows, kHeadDim * 2, kPageSize))) return st;
-  if ((st = encode_rows64(&vmap, v_pages, rows, kHeadDim * 2, kPageSize))) return st;
+  // tensor-core path: K/V as [pages * Hkv * 16, 64] (one 16-row slab per copy) and q as
+  // [total_q tokens, Hq, 64] (one box = one row tile); the chunk kernel reads through pointers
   const int tokens_per_tile = decode_tokens_per_tile(group, std::max(1, ql.max_q));
-  CUtensorMap qmap;  // tensor-core path: q as [total_q tokens, Hq, 64], one box = one row tile
-  if (tensor_cores &&
-      (st = encode_tokens_heads(&qmap, q, (uint64_t)ql.total_q, num_q_heads, tokens_per_tile, group)))
-    return st;
+  CUtensorMap kmap, vmap, qmap;
+  if (tensor_cores) {
+    const uint64_t rows = (uint64_t)num_pages * num_kv_heads * kPageSize;
+    if ((st = encode_rows64(&kmap, k_pages, rows, kHeadDim * 2, kPageSize))) return st;
+    if ((st = encode_rows64(&vmap, v_pages, rows, kHeadDim * 2, kPageSize))) return st;
+    if ((st = encode_tokens_heads(&qmap, q, (uint64_t)ql.total_q, num_q_heads, tokens_per_tile, group))) return st;
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = workspace;
@@ -451,6 +452,9 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.page_table = page_table;
+  p.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
+  p.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
+  p.num_pages = num_pages;
   p.seqlens = seqlens;
   p.sinks = sinks;
   p.out = out;
@@ -479,7 +483,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.withhold_copies = withhold_copies();
-  const cudaError_t e = tensor_cores ? launch_decode_tc(qmap, kmap, vmap, p, s) : launch_decode(kmap, vmap, p, s);
+  const cudaError_t e = tensor_cores ? launch_decode_tc(qmap, kmap, vmap, p, s) : launch_decode(p, s);
   if (owned) cudaFreeAsync(ws, s);
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }

@@ -12,6 +12,9 @@ namespace sa {
 struct DecodeParams {
   const __nv_bfloat16* q;     // [total_q, Hq, 64]: [B, q_len, Hq, 64] or packed by cu_q
   const int32_t* page_table;  // [B, stride]
+  const __nv_bfloat16* k_pages;  // [num_pages, Hkv, 16, 64]: read by the chunk kernel's copies
+  const __nv_bfloat16* v_pages;
+  int num_pages;                  // page ids outside [0, num_pages) read as zeros
   const int32_t* seqlens;     // [B]
   const float* sinks;         // [Hq]
   void* out;                  // [total_q, Hq, 64] bf16 or fp32
@@ -32,7 +35,7 @@ struct DecodeParams {
   int out_f32;
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
-  int withhold_copies;  // failure-path test: the producer issues no copies, so the waits time out
+  int withhold_copies;  // failure-path test: the tensor-core kernel's producer issues no copies, so its waits time out
 };
 
 // Number of chunks sequence with `npages` pages is cut into.  Every chunk is
@@ -47,8 +50,7 @@ __host__ __device__ inline int decode_num_chunks(int npages, int num_splits, int
   return (npages + chunk - 1) / chunk;
 }
 
-__global__ void decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                                    const DecodeParams p);
+__global__ void decode_split_kernel(const DecodeParams p);
 __global__ void decode_merge_kernel(const DecodeParams p);
 
 // Tensor-core variant for many query rows per kv head (multi-token decode):
@@ -68,8 +70,7 @@ int decode_threads();
 cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t stream);
 
 // Enqueue the chunk kernel and, when chunks are merged, the merge kernel.
-cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 // Same with the tensor-core chunk kernel (qmap: q as [B * q_len, Hq, 64],
 // boxes of group heads x tokens_per_tile tokens).
 cudaError_t decode_tc_configure();
