@@ -14,8 +14,9 @@ namespace sa {
 
 // Bits recorded in the device error word.
 enum : unsigned {
-  kErrDecodeFull = 1u << 0,  // a tensor-core decode wait gave up
-  kErrPrefill = 1u << 2,     // any prefill wait gave up
+  kErrDecodeFull = 1u << 0,   // decode consumer waited too long for a page
+  kErrDecodeEmpty = 1u << 1,  // decode producer waited too long for a free stage
+  kErrPrefill = 1u << 2,      // any prefill wait gave up
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
