@@ -57,3 +57,25 @@ def test_two_rank_timing_reduction_and_replicas():
 def test_reduce_max_without_process_group():
     import bench
     assert bench.reduce_max(None, [1.0, 2.0], torch.device("cpu")) == [1.0, 2.0]
+
+
+def test_both_arms_report_the_same_workload():
+    # the reference arm (the oracle on host cores) and the GPU arm name one config, so the two
+    # lines compare the same metric on the same workload
+    import bench
+    for world in (1, 2, 8):
+        cfg = bench._config(world)
+        assert cfg == bench._config(world) and "seq 8192" in cfg["workload"] and "num_splits 8" in cfg["workload"]
+    assert bench._config(1)["parallelism"] == "single GPU" and bench._config(4)["parallelism"] == "replicas x4"
+
+
+def test_traffic_is_reported_only_for_the_captured_source():
+    # the per-launch DRAM bytes come from the committed capture only while the kernel source is
+    # the captured one: any other source hash reads as "not measured"
+    import bench
+    assert bench._traffic("no_such_kernel", bench.PREFILL_SOURCES) is None
+    for line in open(os.path.join(bench.ROOT, "profiles", "dram_traffic.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, digest, nbytes = line.split()[:3]
+        assert len(digest) == 16 and float(nbytes) > 0
