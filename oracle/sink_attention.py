@@ -85,54 +85,72 @@ def _as_int(x) -> np.ndarray:
     return np.asarray(x, dtype=np.int64)
 
 
-def sink_softmax_rows(s: np.ndarray, sink: float):
+def _sink_exp_rows(s: np.ndarray, sink):
+    """Exponentials of a block of rows relative to each row's maximum, the
+    sink included (the second formula of "Sink Attention").
+
+    s    : [r, n] float64 logits (masked entries are -inf)
+    sink : the head's sink logit, one scalar for every row or one per row [r]
+    Returns (e [r, n], e_sink [r], z [r], m [r], empty [r], inf_sink [r]):
+    e = exp(s - m), e_sink = exp(sink - m), z = sum(e) + e_sink, with m the
+    row maximum over the logits and the sink; rows with no finite logit and
+    sink = -inf are flagged ``empty``, rows with sink = +inf ``inf_sink``
+    (their e, e_sink and z are not used).
+    """
+    s = np.asarray(s, dtype=np.float64)
+    r, n = s.shape
+    sink = np.broadcast_to(np.asarray(sink, dtype=np.float64), (r,))
+    row_max = s.max(axis=1) if n > 0 else np.full(r, -math.inf)
+    m = np.maximum(row_max, sink)  # the subtracted maximum includes the sink
+    empty = m == -math.inf
+    inf_sink = sink == math.inf
+    m_safe = np.where(empty | inf_sink, 0.0, m)
+    with np.errstate(over="ignore", invalid="ignore"):
+        e = np.exp(s - m_safe[:, None])
+        e_sink = np.exp(sink - m_safe)
+        z = e.sum(axis=1) + e_sink
+    return e, e_sink, z, m, empty, inf_sink
+
+
+def sink_softmax_rows(s: np.ndarray, sink):
     """Softmax of each row of ``s`` extended by one extra logit ``sink``.
 
     GPT-OSS on day 0, "Sink Attention": softmax of the scaled products with the
     head's sink, evaluated with the maximum subtracted (second formula).
 
     s    : [r, n] float64 logits (masked entries are -inf)
-    sink : scalar logit of the head (may be +-inf)
+    sink : logit of the head (may be +-inf); a scalar, or one per row [r]
     Returns (p [r, n], p_sink [r]) with p.sum(1) + p_sink == 1 for every row
     that has at least one finite logit.  A row with no finite logit and
     sink = -inf has no defined softmax: it returns all zeros (output 0).
     sink = +inf gives p = 0, p_sink = 1 (the limit).
     """
-    s = np.asarray(s, dtype=np.float64)
-    r, n = s.shape
-    if sink == math.inf:
-        return np.zeros_like(s), np.ones(r)
-    row_max = s.max(axis=1) if n > 0 else np.full(r, -math.inf)
-    m = np.maximum(row_max, sink)  # the subtracted maximum includes the sink
-    empty = m == -math.inf
-    m_safe = np.where(empty, 0.0, m)
-    e = np.exp(s - m_safe[:, None])
-    e_sink = np.exp(sink - m_safe)
-    z = e.sum(axis=1) + e_sink
-    z_safe = np.where(empty, 1.0, z)
+    e, e_sink, z, _, empty, inf_sink = _sink_exp_rows(s, sink)
+    z_safe = np.where(empty | inf_sink, 1.0, z)
     p = e / z_safe[:, None]
-    p_sink = np.where(empty, 0.0, e_sink / z_safe)
-    p[empty] = 0.0
+    p_sink = e_sink / z_safe
+    p[empty | inf_sink] = 0.0
+    p_sink = np.where(empty, 0.0, np.where(inf_sink, 1.0, p_sink))
     return p, p_sink
 
 
-def attend_rows(s: np.ndarray, sink: float, v: np.ndarray):
+def attend_rows(s: np.ndarray, sink, v: np.ndarray):
     """Sink attention for a block of query rows sharing one key/value set.
 
-    s : [r, n] scaled logits (masked = -inf), v : [n, D].
-    Returns (out [r, D], lse [r]) where out = p @ v (the sink column is
-    dropped: it has no value vector) and lse = log(sum_j e^s_j + e^sink), the
-    natural-log normaliser including the sink (-inf for an empty row).
+    s : [r, n] scaled logits (masked = -inf), v : [n, D]; sink a scalar or one
+    per row [r].
+    Returns (out [r, D], lse [r]) where out = sum_j e^(s_j - m) v_j / z (the
+    softmax weights times V; the sink column is dropped: it has no value
+    vector) and lse = log(sum_j e^s_j + e^sink), the natural-log normaliser
+    including the sink (-inf for an empty row, +inf for sink = +inf).
     """
-    p, p_sink = sink_softmax_rows(s, sink)
-    out = p @ np.asarray(v, dtype=np.float64)
-    n = s.shape[1]
-    row_max = s.max(axis=1) if n > 0 else np.full(s.shape[0], -math.inf)
-    m = np.maximum(row_max, sink)
+    e, e_sink, z, m, empty, inf_sink = _sink_exp_rows(s, sink)
+    skip = empty | inf_sink
+    z_safe = np.where(skip, 1.0, z)
+    out = (e @ np.asarray(v, dtype=np.float64)) / z_safe[:, None]
+    out[skip] = 0.0
     with np.errstate(divide="ignore", invalid="ignore"):
-        m_safe = np.where(np.isfinite(m), m, 0.0)
-        z = np.exp(s - m_safe[:, None]).sum(axis=1) + np.exp(sink - m_safe)
-        lse = np.where(np.isfinite(m), m_safe + np.log(z), m)
+        lse = np.where(skip, m, m + np.log(z_safe))
     return out, lse
 
 
@@ -145,6 +163,10 @@ def prefill(q, k, v, sinks, cu_seqlens, scale: float):
         s_j = scale * <q[i,h], k[j,g]>   for j = 0..i
         out[i,h] = softmax([s_0..s_i, sinks[h]]) restricted to j, times v[j,g].
     Returns (out [T, Hq, D], lse [T, Hq]).
+
+    Every (token, head) row is an independent softmax; the rows of the query
+    heads that share one kv head are evaluated together, token-major, in
+    blocks of about _ROW_BLOCK rows (to bound memory only).
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     sinks = _as_f64(sinks)
@@ -153,6 +175,7 @@ def prefill(q, k, v, sinks, cu_seqlens, scale: float):
     hkv = k.shape[1]
     assert hq % hkv == 0, "query heads must be a multiple of kv heads"
     group = hq // hkv
+    tokens_per_block = max(1, _ROW_BLOCK // group)
     out = np.zeros((T, hq, d))
     lse = np.full((T, hq), -math.inf)
     for b in range(len(cu) - 1):
@@ -160,20 +183,20 @@ def prefill(q, k, v, sinks, cu_seqlens, scale: float):
         L = t1 - t0
         if L == 0:
             continue
-        for h in range(hq):
-            g = h // group
+        for g in range(hkv):
+            heads = slice(g * group, (g + 1) * group)
             kk = k[t0:t1, g, :]
             vv = v[t0:t1, g, :]
-            for r0 in range(0, L, _ROW_BLOCK):
-                r1 = min(L, r0 + _ROW_BLOCK)
-                # keys beyond r1-1 are masked for every row of this block
-                s = scale * (q[t0 + r0:t0 + r1, h, :] @ kk[:r1].T)
-                rows = np.arange(r0, r1)[:, None]
-                cols = np.arange(r1)[None, :]
-                s = np.where(cols <= rows, s, -math.inf)
-                o, l = attend_rows(s, float(sinks[h]), vv[:r1])
-                out[t0 + r0:t0 + r1, h, :] = o
-                lse[t0 + r0:t0 + r1, h] = l
+            for r0 in range(0, L, tokens_per_block):
+                r1 = min(L, r0 + tokens_per_block)
+                # rows (token i, head h), token-major; keys beyond r1-1 are masked for every row
+                s = scale * (q[t0 + r0:t0 + r1, heads, :].reshape(-1, d) @ kk[:r1].T)
+                tok = np.repeat(np.arange(r0, r1), group)[:, None]
+                cols = np.arange(r0, r1)[None, :]  # only these keys lie past some row's own position
+                s[:, r0:r1] = np.where(cols <= tok, s[:, r0:r1], -math.inf)
+                o, l = attend_rows(s, np.tile(sinks[heads], r1 - r0), vv[:r1])
+                out[t0 + r0:t0 + r1, heads, :] = o.reshape(r1 - r0, group, d)
+                lse[t0 + r0:t0 + r1, heads] = l.reshape(r1 - r0, group)
     return out, lse
 
 
