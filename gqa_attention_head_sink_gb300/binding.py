@@ -45,7 +45,7 @@ EXPORTS = {
     "sink_attn_decode_max_splits": (_I, [_I, _I, _I, _I, _I]),
     "sink_attn_qkv_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P]),
     "sink_attn_yarn_inv_freq": (_I, [_I, ctypes.c_double, ctypes.c_double, _I, ctypes.c_double, ctypes.c_double,
-                                     ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
+                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)]),
     "sink_attn_status_string": (ctypes.c_char_p, [_I]),
     "sink_attn_get_device_error": (_I, [_P]),
     "sink_attn_version": (_I, []),
@@ -120,6 +120,37 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _same_device(ref: torch.Tensor, **tensors):
+    for name, t in tensors.items():
+        if t is not None and t.device != ref.device:
+            raise ValueError(f"{name} is on {t.device}, q on {ref.device}: every tensor must be on one device")
+
+
+def _check_outputs(out, lse, out_shape, lse_shape):
+    """out must be bf16/fp32 with out_shape, lse fp32 with lse_shape: a smaller
+    buffer would be written past its end on the device."""
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    if tuple(out.shape) != tuple(out_shape):
+        raise ValueError(f"out must have shape {tuple(out_shape)}, got {tuple(out.shape)}")
+    if lse is not None and tuple(lse.shape) != tuple(lse_shape):
+        raise ValueError(f"lse must have shape {tuple(lse_shape)}, got {tuple(lse.shape)}")
+    _need(out, "out", out.dtype, len(out_shape))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, len(lse_shape))
+
+
+def _check_paged(q, k_pages, v_pages, page_table, seqlens, sinks, batch, hq, d):
+    """Shapes the paged calls read through: the pools alike, one page-table row
+    and one length per sequence, one sink per query head."""
+    if v_pages.shape != k_pages.shape or k_pages.shape[3] != d:
+        raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
+    if page_table.shape[0] != batch or seqlens.shape[0] != batch:
+        raise ValueError("page_table and seqlens need one row per sequence")
+    if sinks.shape[0] != hq:
+        raise ValueError("sinks must have one entry per query head")
+
+
 def sink_attn_status_string(status: int) -> str:
     return load().sink_attn_status_string(int(status)).decode()
 
@@ -155,11 +186,8 @@ def sink_attn_prefill(q, k, v, sinks, cu_seqlens, scale: float, out=None, out_dt
         max_seqlen = T
     if out is None:
         out = torch.empty((T, hq, d), dtype=out_dtype, device=q.device)
-    if out.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("out must be bf16 or fp32")
-    _need(out, "out", out.dtype, 3)
-    if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+    _check_outputs(out, lse, (T, hq, d), (T, hq))
+    _same_device(q, k=k, v=v, sinks=sinks, cu_seqlens=cu_seqlens, out=out, lse=lse)
     st = load().sink_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), B, T, int(max_seqlen),
                                   hq, hkv, d, float(scale), _ptr(out),
                                   OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse),
@@ -210,18 +238,15 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
     _need(seqlens, "seqlens", torch.int32, 1)
     _need(sinks, "sinks", torch.float32, 1)
     B, hq, d = q.shape
-    num_pages, hkv, page_size, d2 = k_pages.shape
-    if v_pages.shape != k_pages.shape or d2 != d:
-        raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
-    if page_table.shape[0] != B or seqlens.shape[0] != B:
-        raise ValueError("page_table and seqlens need one row per sequence")
+    num_pages, hkv, page_size, _ = k_pages.shape
+    _check_paged(q, k_pages, v_pages, page_table, seqlens, sinks, B, hq, d)
     if max_seqlen is None:  # the page-table width bounds every length: no device read
         max_seqlen = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
-    _need(out, "out", out.dtype, 3)
-    if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+    _check_outputs(out, lse, (B, hq, d), (B, hq))
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, page_table=page_table, seqlens=seqlens, sinks=sinks,
+                 out=out, lse=lse, workspace=workspace)
     if workspace is None:
         workspace = _workspace(load().sink_attn_decode_workspace_bytes(B, int(max_seqlen), hq, hkv, d, page_size,
                                                                        int(num_splits)), q.device, stream)
@@ -252,18 +277,15 @@ def sink_attn_decode_multi(q, k_pages, v_pages, page_table, seqlens, sinks, scal
     _need(seqlens, "seqlens", torch.int32, 1)
     _need(sinks, "sinks", torch.float32, 1)
     B, n, hq, d = q.shape
-    num_pages, hkv, page_size, d2 = k_pages.shape
-    if v_pages.shape != k_pages.shape or d2 != d:
-        raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
-    if page_table.shape[0] != B or seqlens.shape[0] != B:
-        raise ValueError("page_table and seqlens need one row per sequence")
+    num_pages, hkv, page_size, _ = k_pages.shape
+    _check_paged(q, k_pages, v_pages, page_table, seqlens, sinks, B, hq, d)
     if max_seqlen is None:  # the page-table width bounds every length: no device read
         max_seqlen = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((B, n, hq, d), dtype=out_dtype, device=q.device)
-    _need(out, "out", out.dtype, 4)
-    if lse is not None:
-        _need(lse, "lse", torch.float32, 3)
+    _check_outputs(out, lse, (B, n, hq, d), (B, n, hq))
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, page_table=page_table, seqlens=seqlens, sinks=sinks,
+                 out=out, lse=lse, workspace=workspace)
     if workspace is None:
         workspace = _workspace(load().sink_attn_decode_multi_workspace_bytes(B, n, int(max_seqlen), hq, hkv, d,
                                                                              page_size, int(num_splits)),
@@ -307,12 +329,11 @@ def sink_attn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqle
     _need(seqlens_k, "seqlens_k", torch.int32, 1)
     _need(sinks, "sinks", torch.float32, 1)
     total_q, hq, d = q.shape
-    num_pages, hkv, page_size, d2 = k_pages.shape
+    num_pages, hkv, page_size, _ = k_pages.shape
     B = seqlens_k.shape[0]
-    if v_pages.shape != k_pages.shape or d2 != d:
-        raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D]")
-    if page_table.shape[0] != B or cu_seqlens_q.shape[0] != B + 1:
-        raise ValueError("page_table needs one row and cu_seqlens_q one offset per sequence (plus one)")
+    _check_paged(q, k_pages, v_pages, page_table, seqlens_k, sinks, B, hq, d)
+    if cu_seqlens_q.shape[0] != B + 1:
+        raise ValueError("cu_seqlens_q needs one offset per sequence (plus one)")
     # upper bounds known without reading the device (graph-capturable); pass the true
     # maxima to size the work exactly
     if max_seqlen_q is None:
@@ -321,9 +342,9 @@ def sink_attn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqle
         max_seqlen_k = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((total_q, hq, d), dtype=out_dtype, device=q.device)
-    _need(out, "out", out.dtype, 3)
-    if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+    _check_outputs(out, lse, (total_q, hq, d), (total_q, hq))
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, page_table=page_table, cu_seqlens_q=cu_seqlens_q,
+                 seqlens_k=seqlens_k, sinks=sinks, out=out, lse=lse, workspace=workspace)
     if workspace is None:
         workspace = _workspace(load().sink_attn_prefill_paged_workspace_bytes(B, total_q, int(max_seqlen_q),
                                                                               int(max_seqlen_k), hq, hkv, d,
@@ -345,15 +366,15 @@ def sink_attn_prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqle
 def sink_attn_yarn_inv_freq(head_dim: int = 64, base: float = 10000.0, factor: float = 1.0,
                             original_max_position: int = 4096, beta_fast: float = 32.0, beta_slow: float = 1.0):
     """YaRN rotary frequencies (host computation in the library).  Returns
-    (inv_freq as a CPU float32 tensor [head_dim / 2], attn_factor)."""
+    (inv_freq as a CPU float64 tensor [head_dim / 2], attn_factor)."""
     if head_dim <= 0 or head_dim % 2:
         raise SinkAttnError(1, "sink_attn_yarn_inv_freq")
-    buf = (ctypes.c_float * (head_dim // 2))()
+    buf = (ctypes.c_double * (head_dim // 2))()
     af = ctypes.c_float()
     st = load().sink_attn_yarn_inv_freq(head_dim, float(base), float(factor), int(original_max_position),
                                         float(beta_fast), float(beta_slow), buf, ctypes.byref(af))
     _check(st, "sink_attn_yarn_inv_freq")
-    return torch.tensor(list(buf), dtype=torch.float32), float(af.value)
+    return torch.tensor(list(buf), dtype=torch.float64), float(af.value)
 
 
 def sink_attn_qkv_rope(q, k, v, positions, inv_freq, attn_factor: float = 1.0, q_bias=None, k_bias=None,
@@ -361,13 +382,13 @@ def sink_attn_qkv_rope(q, k, v, positions, inv_freq, attn_factor: float = 1.0, q
     """In place: q <- rot(q + q_bias), k <- rot(k + k_bias), v <- v + v_bias,
     rotation by positions[t] * inv_freq (half-split planes) times attn_factor.
     q [T,Hq,64], k/v [T,Hkv,64] bf16; biases [H,64] bf16 or None; positions [T]
-    int32; inv_freq [32] fp32 (CUDA).  With slot_mapping [T] int32 the new k/v
+    int32; inv_freq [32] fp64 (CUDA).  With slot_mapping [T] int32 the new k/v
     are also written to k_pages/v_pages [num_pages,Hkv,16,64] at those slots."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
     _need(positions, "positions", torch.int32, 1)
-    _need(inv_freq, "inv_freq", torch.float32, 1)
+    _need(inv_freq, "inv_freq", torch.float64, 1)
     for name, b in (("q_bias", q_bias), ("k_bias", k_bias), ("v_bias", v_bias)):
         if b is not None:
             _need(b, name, torch.bfloat16, 2)
@@ -408,13 +429,14 @@ def sink_attn_decode_noalloc(q, k_pages, v_pages, page_table, seqlens, sinks, sc
     _need(sinks, "sinks", torch.float32, 1)
     B, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_pages.shape
+    _check_paged(q, k_pages, v_pages, page_table, seqlens, sinks, B, hq, d)
     if max_seqlen is None:  # the page-table width bounds every length: no device read
         max_seqlen = page_table.shape[1] * page_size
     if out is None:
         out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
-    _need(out, "out", out.dtype, 3)
-    if lse is not None:
-        _need(lse, "lse", torch.float32, 2)
+    _check_outputs(out, lse, (B, hq, d), (B, hq))
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, page_table=page_table, seqlens=seqlens, sinks=sinks,
+                 out=out, lse=lse)
     st = load().sink_attn_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                                          page_table.shape[1], _ptr(seqlens), B, int(max_seqlen), num_pages,
                                          _ptr(sinks), hq, hkv, d, page_size, float(scale), int(num_splits), _ptr(out),

@@ -61,8 +61,10 @@ extern "C" int sink_attn_decode_noalloc(const void* q, const void* k_pages, cons
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != SINK_ATTN_OK) return st;
-  // The chunk kernel writes every partial slot the merge reads, so the
-  // contents left by an earlier call never need clearing.
+  // Every partial slot the merge kernel reads is written by this call's chunk
+  // kernel first (one query token per sequence runs on the split kernel, which
+  // has no bounded wait that could give up half way), so the contents left by
+  // an earlier call never need clearing.
   return sink_attn_decode(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, max_seqlen, num_pages,
                           sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out, out_dtype,
                           lse, scratch, (size_t)SINK_ATTN_NOALLOC_SCRATCH_BYTES, stream);

@@ -224,12 +224,15 @@ def test_prefill_paged_workspace(lib):
 
 def test_yarn_inv_freq_matches_the_oracle(lib):
     import numpy as np
+    import torch
+
     import oracle
     for args in [(64, 150000.0, 32.0, 4096, 32.0, 1.0), (64, 10000.0, 1.0, 4096, 32.0, 1.0),
                  (128, 500000.0, 8.0, 8192, 16.0, 2.0)]:
         f, af = sa.sink_attn_yarn_inv_freq(*args)
         want, want_af = oracle.yarn_inv_freq(*args)
-        np.testing.assert_allclose(f.numpy(), want, rtol=2.0 ** -24, atol=0)
+        assert f.dtype == torch.float64
+        np.testing.assert_allclose(f.numpy(), want, rtol=2.0 ** -50, atol=0)
         assert abs(af - want_af) <= 2.0 ** -23 * want_af
 
 
@@ -288,3 +291,36 @@ def test_binding_signatures_match_the_header():
     assert set(arities) == set(binding.EXPORTS), set(arities) ^ set(binding.EXPORTS)
     for name, (_, args) in binding.EXPORTS.items():
         assert len(args) == arities[name], f"{name}: binding has {len(args)} arguments, header {arities[name]}"
+
+
+def test_paged_shape_checks_reject_mismatches_before_any_launch():
+    # the C ABI takes the pool size from k_pages and the batch from q, so a short v_pool,
+    # page table, length vector or sink vector would be read past its end on the device:
+    # the binding refuses them first (shapes only; no device is touched)
+    import torch
+    q = torch.empty(4, 16, 64)
+    kp = torch.empty(10, 2, 16, 64)
+    table, lens, sinks = torch.empty(4, 3), torch.empty(4), torch.empty(16)
+    binding._check_paged(q, kp, kp, table, lens, sinks, 4, 16, 64)  # consistent: passes
+    bad = [
+        dict(v_pages=torch.empty(9, 2, 16, 64)),
+        dict(page_table=torch.empty(3, 3)),
+        dict(seqlens=torch.empty(3)),
+        dict(sinks=torch.empty(8)),
+    ]
+    for kw in bad:
+        args = dict(q=q, k_pages=kp, v_pages=kp, page_table=table, seqlens=lens, sinks=sinks)
+        args.update(kw)
+        with pytest.raises(ValueError):
+            binding._check_paged(args["q"], args["k_pages"], args["v_pages"], args["page_table"], args["seqlens"],
+                                 args["sinks"], 4, 16, 64)
+
+
+@pytest.mark.parametrize("out_shape,lse_shape", [((4, 16, 63), None), ((3, 16, 64), None), ((4, 16, 64), (4, 15)),
+                                                 ((4, 16, 64), (4, 16, 1))])
+def test_output_shape_checks_reject_short_buffers(out_shape, lse_shape):
+    import torch
+    out = torch.empty(*out_shape)
+    lse = None if lse_shape is None else torch.empty(*lse_shape)
+    with pytest.raises(ValueError, match="shape"):
+        binding._check_outputs(out, lse, (4, 16, 64), (4, 16))

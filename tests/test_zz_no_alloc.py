@@ -64,3 +64,30 @@ def test_noalloc_rejects_partials_beyond_the_scratch_size(lib):
     st = lib.sink_attn_decode_noalloc(fake(256), fake(512), fake(768), fake(1024), 2048, fake(1280), 128, 32768,
                                       1 << 18, fake(1536), 64, 8, 64, 16, 0.125, 16, fake(1792), 1, None, None)
     assert st == 2  # SINK_ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_noalloc_single_chunk_and_wide_groups(lib):
+    # one chunk per sequence: the chunks write the output directly and no partial
+    # state reaches the scratch array; still the same results as sink_attn_decode
+    inp = workloads.make_decode([700, 5, 4096], num_q_heads=16, num_kv_heads=1, seed=33, sink_mode="mixed",
+                                num_splits=1, device="cuda")
+    assert sa.sink_attn_decode_workspace_bytes(inp.batch, inp.max_seqlen, 16, 1, 64, 16, 1) == 0
+    got = sa.sink_attn_decode_noalloc(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.seqlens_t, inp.sinks,
+                                      inp.scale, num_splits=1, max_seqlen=inp.max_seqlen)
+    ref = sa.sink_attn_decode(inp.q, inp.k_pages, inp.v_pages, inp.page_table, inp.seqlens_t, inp.sinks, inp.scale,
+                              num_splits=1, max_seqlen=inp.max_seqlen)
+    torch.cuda.synchronize()
+    _close(got, ref)
+    want, _ = oracle.decode(inp.q.cpu(), inp.k_pages.cpu(), inp.v_pages.cpu(), inp.page_table.cpu(),
+                            inp.seqlens_t.cpu(), inp.sinks.cpu(), inp.scale)
+    assert_parity(got, want)
+    # a group of 32 query heads per kv head is outside what one-token decode supports,
+    # with or without the scratch array: refused on the host with the same status
+    wide = workloads.make_decode([64, 32], num_q_heads=64, num_kv_heads=2, seed=34, device="cuda")
+    for fn in (sa.sink_attn_decode_noalloc, sa.sink_attn_decode):
+        with pytest.raises(sa.SinkAttnError) as e:
+            fn(wide.q, wide.k_pages, wide.v_pages, wide.page_table, wide.seqlens_t, wide.sinks, wide.scale,
+               num_splits=2, max_seqlen=wide.max_seqlen)
+        assert e.value.status == 2
+    assert sa.sink_attn_get_device_error() == 0
