@@ -494,7 +494,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
 extern "C" {
 
 int sink_attn_yarn_inv_freq(int head_dim, double base, double factor, int original_max_position, double beta_fast,
-                            double beta_slow, float* inv_freq, float* attn_factor) {
+                            double beta_slow, double* inv_freq, float* attn_factor) {
   if (!inv_freq || !attn_factor || head_dim <= 0 || head_dim % 2) return SINK_ATTN_ERR_INVALID_ARG;
   if (!(base > 1.0) || !std::isfinite(base) || !(factor > 0.0) || !std::isfinite(factor))
     return SINK_ATTN_ERR_INVALID_ARG;
@@ -511,14 +511,14 @@ int sink_attn_yarn_inv_freq(int head_dim, double base, double factor, int origin
       const double ramp = std::min(1.0, std::max(0.0, (turns - beta_slow) / (beta_fast - beta_slow)));
       f = (1.0 - ramp) * theta / factor + ramp * theta;
     }
-    inv_freq[i] = (float)f;
+    inv_freq[i] = f;
   }
   *attn_factor = factor > 1.0 ? (float)(0.1 * std::log(factor) + 1.0) : 1.0f;
   return SINK_ATTN_OK;
 }
 
 int sink_attn_qkv_rope(void* q, void* k, void* v, const void* q_bias, const void* k_bias, const void* v_bias,
-                       const int32_t* positions, const float* inv_freq, float attn_factor, int num_tokens,
+                       const int32_t* positions, const double* inv_freq, float attn_factor, int num_tokens,
                        int num_q_heads, int num_kv_heads, int head_dim, const int32_t* slot_mapping,
                        void* k_pages, void* v_pages, int num_pages, int page_size, void* stream) {
   if (num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0) return SINK_ATTN_ERR_INVALID_ARG;

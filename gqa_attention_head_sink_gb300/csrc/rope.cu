@@ -20,12 +20,11 @@
 // cache slots, so the attention kernels read the cache unchanged.
 //
 // One CTA per 8 tokens: each thread first forms one (token, plane) entry of
-// the cos/sin table (the angle position * inv_freq in fp64 -- exact for int32
-// positions and fp32 frequencies -- reduced to [-pi, pi] before a
-// single-precision sincos, so large positions keep full accuracy); then the
-// threads take (token, head, lane) items, a lane rotating 8 planes of one head
-// row with 16-byte loads of both halves, and v rows get their bias in 16-byte
-// pieces.
+// the cos/sin table (the angle position * inv_freq as a 64-bit fixed-point
+// phase, exact modulo one turn for any int32 position, then sincospif; see
+// rope_cos_sin), then the threads take (token, head, lane) items, a lane
+// rotating 8 planes of one head row with 16-byte loads of both halves, and v
+// rows get their bias in 16-byte pieces.
 #include "common.cuh"
 #include "rope.h"
 
@@ -59,18 +58,18 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 
 __global__ void __launch_bounds__(kThreads) qkv_rope_kernel(const RopeParams p) {
   __shared__ float cs[kTokensPerBlock][kHalf], sn[kTokensPerBlock][kHalf];
+  __shared__ unsigned long long turn[kHalf];
   __shared__ long long cache_row[kTokensPerBlock];
   const int tid = threadIdx.x;
   const int t_base = blockIdx.x * kTokensPerBlock;
+  if (tid < kHalf) turn[tid] = rope_turn_increment(__ldg(p.inv_freq + tid));
+  __syncthreads();
   {
     // one (token, plane) angle per thread: 8 tokens x 32 planes = 256
     const int tb = tid / kHalf, i = tid % kHalf, t = t_base + tb;
     if (t < p.tokens) {
-      const double angle = (double)__ldg(p.positions + t) * (double)__ldg(p.inv_freq + i);
-      const double two_pi = 6.283185307179586476925286766559;
-      const double reduced = angle - two_pi * rint(angle / two_pi);  // in [-pi, pi]
       float s, c;
-      sincosf((float)reduced, &s, &c);
+      rope_cos_sin(__ldg(p.positions + t), turn[i], c, s);
       cs[tb][i] = c * p.attn_factor;
       sn[tb][i] = s * p.attn_factor;
     }

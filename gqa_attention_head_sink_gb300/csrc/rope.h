@@ -15,7 +15,7 @@ struct RopeParams {
   const __nv_bfloat16* k_bias;  // [hkv, 64] or null
   const __nv_bfloat16* v_bias;  // [hkv, 64] or null
   const int32_t* positions;     // [tokens]
-  const float* inv_freq;        // [32] rotation frequency of each plane
+  const double* inv_freq;       // [32] rotation frequency of each plane (radians per position)
   float attn_factor;            // multiplies the rotated q and k
   const int32_t* slot_mapping;  // [tokens] cache slot (page * page_size + offset) or null; < 0 skips
   __nv_bfloat16* k_pages;       // [num_pages, hkv, page_size, 64] when slot_mapping is set
@@ -23,6 +23,27 @@ struct RopeParams {
   int num_pages, page_size;
   int tokens, hq, hkv;
 };
+
+// Rotation angles without fp64 arithmetic per element.  A plane's frequency f
+// (radians per position) is turned once into a 64-bit fixed-point fraction of
+// a turn, F = frac(f / 2 pi) * 2^64; the phase of position p is then the
+// integer product p * F taken modulo 2^64, which is p * f modulo one turn with
+// no rounding beyond that of F (a relative 2^-53, the precision of the fp64
+// frequency itself).  The top 32 bits, read as a signed fraction of a half
+// turn, go to sincospif.
+__device__ __forceinline__ unsigned long long rope_turn_increment(double f) {
+  double t = f / 6.283185307179586476925286766559;
+  t -= floor(t);  // [0, 1]: whole turns contribute nothing
+  const double scaled = t * 18446744073709551616.0;  // 2^64
+  return scaled >= 18446744073709551616.0 ? 0ull : __double2ull_rn(scaled);
+}
+
+// cos and sin of the angle position * f, F = rope_turn_increment(f).
+__device__ __forceinline__ void rope_cos_sin(int position, unsigned long long F, float& c, float& s) {
+  const unsigned long long phase = (unsigned long long)(long long)position * F;  // modulo 2^64 = one turn
+  const float half_turns = (float)(int)(phase >> 32) * 0x1p-31f;                 // in [-1, 1)
+  sincospif(half_turns, &s, &c);
+}
 
 __global__ void qkv_rope_kernel(const RopeParams p);
 cudaError_t launch_qkv_rope(const RopeParams& p, cudaStream_t stream);

@@ -75,9 +75,10 @@ typedef enum {
  *               host copies used to size the grid without a device sync;
  *               max_seqlen must be >= every sequence length.
  *   scale       softmax scale applied to q.k (typically 1/sqrt(head_dim)).
- *               k and v must be finite everywhere: key tiles are 128 tokens
- *               long, and the tail of a sequence's last tile (tokens of the next
- *               sequence) enters the value product with weight exactly 0.
+ *               A sequence's output depends on its own q, k and v only: the
+ *               next packed sequence's tokens, which share its last 128-key
+ *               tile, are masked and their values zeroed before the product,
+ *               so even NaN or Inf there does not reach it.
  *   out         [total_tokens, num_q_heads, head_dim], bf16 or fp32 per
  *               out_dtype.  Written for every token of every sequence.
  *   lse         optional fp32 [total_tokens, num_q_heads] (natural-log
@@ -270,7 +271,12 @@ int sink_attn_decode_max_splits(int batch, int max_seqlen, int num_kv_heads, int
  *     nothing in it needs clearing between calls.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: resetting the device (cudaDeviceReset) after that first call is
+ *     not supported.
+ *   - If any call reported SINK_ATTN_ERR_TIMEOUT through
+ *     sink_attn_get_device_error(), the outputs of the calls it covers are
+ *     undefined.
  */
 #define SINK_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -291,9 +297,12 @@ int sink_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_p
  *   q[t,h] <- rot(q[t,h] + q_bias[h]),  k[t,g] <- rot(k[t,g] + k_bias[g]),
  *   v[t,g] <- v[t,g] + v_bias[g]
  * where rot rotates each plane (dim i, dim i + D/2) by the angle
- * positions[t] * inv_freq[i] (computed without rounding: fp64 product, then
- * reduced to [-pi, pi]) and multiplies the result by attn_factor; the sum
- * and rotation run in fp32, the result is rounded once to bf16.
+ * positions[t] * inv_freq[i] and multiplies the result by attn_factor.  The
+ * angle is formed modulo one turn as a 64-bit fixed-point product of the
+ * position and the frequency (in turns per position, from the fp64 table),
+ * so it keeps the precision of the fp64 frequency at every int32 position
+ * (within ~1e-7 rad before sincospif); the sum and rotation run in fp32, the
+ * result is rounded once to bf16.
  *
  *   q, k, v     bf16 [num_tokens, H, head_dim] (H = num_q_heads for q,
  *               num_kv_heads for k and v), DEVICE, modified in place
@@ -301,7 +310,8 @@ int sink_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_p
  *               bf16 [H, head_dim] DEVICE, or NULL for no bias
  *   positions   int32 [num_tokens] DEVICE: position of each token in its
  *               sequence (e.g. L - n + t for the n new tokens of a cache of L)
- *   inv_freq    fp32 [head_dim / 2] DEVICE (sink_attn_yarn_inv_freq fills it)
+ *   inv_freq    fp64 [head_dim / 2] DEVICE, radians per position
+ *               (sink_attn_yarn_inv_freq fills it)
  *   attn_factor YaRN's temperature (sink_attn_yarn_inv_freq), 1 for plain RoPE
  *   slot_mapping
  *               optional int32 [num_tokens] DEVICE: cache slot (page *
@@ -313,7 +323,7 @@ int sink_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_p
  * num_tokens == 0 is a no-op returning SINK_ATTN_OK.
  */
 int sink_attn_qkv_rope(void* q, void* k, void* v, const void* q_bias, const void* k_bias,
-                       const void* v_bias, const int32_t* positions, const float* inv_freq,
+                       const void* v_bias, const int32_t* positions, const double* inv_freq,
                        float attn_factor, int num_tokens, int num_q_heads, int num_kv_heads,
                        int head_dim, const int32_t* slot_mapping, void* k_pages, void* v_pages,
                        int num_pages, int page_size, void* stream);
@@ -326,13 +336,13 @@ int sink_attn_qkv_rope(void* q, void* k, void* v, const void* q_bias, const void
  * beta_slow), 0, 1) and the frequency becomes (1 - g) theta_i / s + g theta_i
  * (YaRN's "NTK-by-parts" interpolation, linear in r as the YaRN paper writes
  * it); attn_factor = 0.1 ln(s) + 1.  s <= 1 gives plain RoPE and 1.
- *   inv_freq     HOST fp32 [head_dim / 2], written
+ *   inv_freq     HOST fp64 [head_dim / 2], written
  *   attn_factor  HOST fp32, written
  * Returns SINK_ATTN_ERR_INVALID_ARG for odd head_dim, base <= 1, factor <= 0,
  * or (factor > 1) original_max_position <= 0 or not 0 < beta_slow < beta_fast.
  */
 int sink_attn_yarn_inv_freq(int head_dim, double base, double factor, int original_max_position,
-                            double beta_fast, double beta_slow, float* inv_freq,
+                            double beta_fast, double beta_slow, double* inv_freq,
                             float* attn_factor);
 
 /* Static, human-readable name of a status code (never NULL). */

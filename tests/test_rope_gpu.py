@@ -5,8 +5,10 @@ frequency, times YaRN's temperature) after adding their biases, biases v,
 and optionally appends the new k and v to the paged cache.  Outputs are
 bf16: each element may differ from the float64 value by one bf16 spacing
 (the single rounding of the result, which a last-bit difference of the fp32
-arithmetic can push to the other neighbour).  Positions reach 2^20, where an
-fp32 angle would already be off by 0.03 rad.  The end-to-end test runs the
+arithmetic can push to the other neighbour).  The expected values use the
+oracle's float64 YaRN table, the kernel the library's fp64 table: the angle the
+kernel forms must keep that precision at every int32 position, up to 2^31 - 1.
+The end-to-end test runs the
 pass and then prefill, against the oracle's float64 pass, rounded once to
 bf16 (the pass's output type, which attention consumes), followed by its
 prefill.  All calls go through the C ABI.
@@ -49,12 +51,17 @@ def _close_bf16(got, want):
     (300, 64, 8, (150000.0, 32.0, 4096, 32.0, 1.0), True, 1 << 20),
     (77, 8, 8, (10000.0, 1.0, 4096, 32.0, 1.0), False, 4096),
     (129, 16, 1, (500000.0, 8.0, 8192, 16.0, 2.0), True, 70000),
+    (256, 64, 8, (150000.0, 32.0, 4096, 32.0, 1.0), True, 1 << 24),
+    (200, 16, 2, (150000.0, 32.0, 4096, 32.0, 1.0), True, (1 << 31) - 1),
+    (100, 16, 2, (10000.0, 1.0, 4096, 32.0, 1.0), True, (1 << 31) - 1),
 ])
 def test_qkv_rope_matches_oracle(T, hq, hkv, yarn, with_bias, max_pos):
     q, k, v, (bq, bk, bv) = _inputs(T, hq, hkv, seed=T + hq)
     pos = torch.randint(0, max_pos, (T,), generator=torch.Generator().manual_seed(T), dtype=torch.int32)
-    f, af = sa.sink_attn_yarn_inv_freq(64, *yarn)
-    want_q, want_k, want_v = oracle.qkv_bias_rope(q, k, v, bq, bk, bv, pos, f, af)
+    pos[0] = max_pos - 1  # the largest position of the range is always there
+    f, af = sa.sink_attn_yarn_inv_freq(64, *yarn)  # the library's fp64 table goes to the kernel
+    f64, af64 = oracle.yarn_inv_freq(64, *yarn)     # the expected values use the oracle's own table
+    want_q, want_k, want_v = oracle.qkv_bias_rope(q, k, v, bq, bk, bv, pos, f64, af64)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     cu = lambda t: None if t is None else t.cuda()  # noqa: E731
     sa.sink_attn_qkv_rope(dq, dk, dv, pos.cuda(), f.cuda(), af, cu(bq), cu(bk), cu(bv))
@@ -99,7 +106,8 @@ def test_bias_rope_then_prefill_matches_oracle():
     bv = (0.5 * torch.randn(8, 64, generator=g)).to(torch.bfloat16)
     pos = torch.cat([torch.arange(L, dtype=torch.int32) for L in lens])
     f, af = sa.sink_attn_yarn_inv_freq(64, 150000.0, 32.0, 4096, 32.0, 1.0)
-    q2, k2, v2 = oracle.qkv_bias_rope(inp.q, inp.k, inp.v, bq, bk, bv, pos, f, af)
+    f64, af64 = oracle.yarn_inv_freq(64, 150000.0, 32.0, 4096, 32.0, 1.0)
+    q2, k2, v2 = oracle.qkv_bias_rope(inp.q, inp.k, inp.v, bq, bk, bv, pos, f64, af64)
     # the pass hands bf16 q, k, v to attention: round the float64 results once
     # (nearest even), as the pass's contract says, then take the attention
     r = lambda x: torch.from_numpy(x).to(torch.bfloat16)  # noqa: E731
