@@ -47,10 +47,11 @@
 // are gathered as 8 page slabs (2 KiB TMA copies, 8 per tile); a unit needs
 // the key tiles up to its last row's position; the causal mask applies to
 // every tile that crosses a row's last key; rows may see no key at all (more
-// query rows than cached tokens), which the softmax guards; V rows past the
-// last needed key are zeroed before the last PV (stale or poisoned slots must
-// not meet a zero weight inside the MMA).  The contiguous path compiles
-// without any of it.
+// query rows than cached tokens), which the softmax guards.  In both modes V
+// rows past the last needed key are zeroed before the last PV: stale or
+// poisoned slots, or the next packed sequence's tokens, must not meet a zero
+// weight inside the MMA (0 x NaN = NaN), so a sequence's output never depends
+// on another sequence's values.
 #include "common.cuh"
 #include "prefill.h"
 #include "tcgen05.cuh"
@@ -185,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* total_qblocks = reinterpret_cast<int*>(smem + kOffMisc + 8);
-  // paged mode: tail-V zeroings head 0's MMA warp has finished (head 1's waits on the count,
-  // which cannot alias the way a phase bit could when head 0 runs a unit ahead)
+  // tail-V zeroings head 0's MMA warp has finished (head 1's waits on the count, which
+  // cannot alias the way a phase bit could when head 0 runs a unit ahead)
   volatile int* zeroed_count = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
   int* seq_start = reinterpret_cast<int*>(smem + kOffSeq);   // sorted
   int* seq_len = seq_start + kPrefillMaxBatch;                // sorted
@@ -362,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, abort_flag));
     };
     const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t), a_p = tmem + col_p(t);
-    int zeroings = 0;  // paged mode: tail-V zeroings met so far
+    int zeroings = 0;  // tail-V zeroings met so far
     Unit u;
     bool ok = true;
     for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
@@ -410,11 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_all(bars.p_full + t, pph))) break;
         pph ^= 1;
         tc_fence_after();
-        if constexpr (kPaged) {
-          const int valid = kend - j * kTile;  // keys of this tile the unit needs
+        {
+          // keys of this tile the unit needs: paged mode, up to its last row's position;
+          // contiguous mode, up to the sequence end (only the last query block's
+          // diagonal tile can end early, when the length is not a multiple of 128)
+          const int valid = (kPaged ? kend : seq_len[u.seq]) - j * kTile;
           if (valid < kTile) {
-            // rows past them: slabs not copied or slots past the sequence end.  Head 0's
-            // warp zeroes them (fence for the tensor core's reads); head 1's waits for it.
+            // rows past them (slabs not copied, slots past the sequence end, or the next
+            // packed sequence's tokens) enter the product with weight 0, and 0 x NaN is NaN:
+            // head 0's warp zeroes them (fence for the tensor core's reads); head 1's waits.
             ++zeroings;
             if (t == 0) {
               uint4* vrows = reinterpret_cast<uint4*>(ring + (vi % kSlots) * kTileBytes);

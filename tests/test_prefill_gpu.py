@@ -2,10 +2,10 @@
 
 All calls go through the C ABI.  Small and medium cases (several 128-row
 tiles, ragged tails, empty and one-token sequences, odd GQA groups, every
-sink edge case) are compared on every element; the full-size workloads
-(one 8192-token sequence with 64/8 heads, and 16 ragged sequences of
-256..32768 tokens) are compared on sampled rows covering tile boundaries,
-sequence starts and ends, for every head.
+sink edge case) are compared on every element, and so are the full-size
+workloads (one 8192-token sequence with 64/8 heads, and 16 ragged sequences
+of 256..32768 tokens), with the mean error taken over the whole workload; a
+131072-token sequence is compared on sampled rows.
 """
 import numpy as np
 import pytest
@@ -14,6 +14,7 @@ import torch
 import gqa_attention_head_sink_gb300 as sa
 import oracle
 from gqa_attention_head_sink_gb300 import build, workloads
+from tests.full_parity import check_prefill_everywhere
 from tests.parity import assert_parity, lse_close
 
 pytestmark = pytest.mark.gpu
@@ -108,29 +109,45 @@ def test_prefill_sequences_do_not_leak_into_each_other():
     assert torch.equal(a[:300], b[:300])
 
 
+@pytest.mark.parametrize("poison", [float("nan"), float("inf"), -float("inf")])
+def test_prefill_packed_neighbours_may_hold_non_finite_values(poison):
+    # the first sequence (300 = 2 x 128 + 44 tokens) shares its last key tile with the
+    # second one's first 84 tokens; whatever those hold, even NaN or Inf, the first
+    # sequence's output must equal the clean run and the oracle
+    lens = [300, 260, 129]
+    inp = workloads.make_prefill(lens, num_q_heads=16, num_kv_heads=2, seed=15, sink_mode="mixed", device="cuda")
+    want, want_lse = full_oracle(inp)
+    clean, clean_lse = run(inp, with_lse=True)
+    inp.k[300:560] = poison
+    inp.v[300:560] = poison
+    dirty, dirty_lse = run(inp, with_lse=True)
+    for out, lse in ((clean, clean_lse), (dirty, dirty_lse)):
+        assert_parity(out[:300], want[:300])
+        lse_close(lse[:300], want_lse[:300])
+        assert_parity(out[560:], want[560:])  # the third sequence reads none of the poisoned tokens
+    assert torch.equal(clean[:300], dirty[:300]) and torch.equal(clean[560:], dirty[560:])
+
+
 @pytest.mark.slow
-def test_prefill_full_len8192():
+def test_prefill_full_len8192_every_element():
+    # the 8192-token gpt-oss prefill: every row and head, fp32 and bf16 output and the lse,
+    # against the float64 oracle (about 0.55 TFLOP of float64 work, spread over the host cores)
     inp = workloads.workload("gptoss_prefill", device="cuda")
-    out, lse = run(inp, with_lse=True)
-    toks = sampled_rows(inp.seqlens, extra=(1000, 4095, 4096, 6000))
-    heads = list(range(inp.num_q_heads))
-    cpu = (inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu())
-    want, want_lse = oracle.prefill_rows(*cpu, inp.scale, toks, heads)
-    assert_parity(out[toks], want)
-    lse_close(lse[toks], want_lse)
+    out32, lse = run(inp, with_lse=True)
+    out16, _ = run(inp, out_dtype=torch.bfloat16)
+    total = check_prefill_everywhere(inp, out32=out32, out16=out16, lse=lse)
+    assert total["out32"]["n"] == inp.total_tokens * inp.num_q_heads * 64
 
 
 @pytest.mark.slow
-def test_prefill_full_ragged16():
+def test_prefill_full_ragged16_every_element():
+    # 16 ragged sequences (215586 tokens, sinks -inf / 0 / N(0,2) / +20 by head): every row and
+    # head, fp32 and bf16 output and the lse (about 34 TFLOP of float64 work over the host cores)
     inp = workloads.workload("ragged_prefill", device="cuda")
-    out, _ = run(inp)
-    toks = sampled_rows(inp.seqlens)
-    rng = np.random.default_rng(0)
-    toks = sorted(rng.choice(toks, size=min(len(toks), 96), replace=False).tolist())
-    heads = list(range(inp.num_q_heads))
-    cpu = (inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.sinks.cpu(), inp.cu_seqlens.cpu())
-    want, _ = oracle.prefill_rows(*cpu, inp.scale, toks, heads)
-    assert_parity(out[toks], want)
+    out32, lse = run(inp, with_lse=True)
+    out16, _ = run(inp, out_dtype=torch.bfloat16)
+    total = check_prefill_everywhere(inp, out32=out32, out16=out16, lse=lse)
+    assert total["out32"]["n"] == inp.total_tokens * inp.num_q_heads * 64
 
 
 @pytest.mark.slow
