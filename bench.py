@@ -8,6 +8,10 @@ One step = one pass of the whole hot path over one batch of synthetic input:
   * decode: 64 sequences x 8192 cached tokens, one query each, paged bf16 KV
     (16-token pages, randomly permuted page table), 8 chunks per sequence,
     merged.
+After the timed steps, the two largest workloads are timed per call, each
+with its own roofline line: `long_decode` (128 sequences of 16384..32768
+cached tokens) and `ragged_prefill` (16 packed sequences of 256..32768
+tokens); then the rows built beyond the hot path (`next_rows`).
 Inputs are resident in HBM before timing starts.  Between timed steps a
 256 MiB buffer is written to flush L2 (the prefill's 80 MiB of inputs would
 otherwise stay cached); the flush is outside the timed events.
@@ -248,6 +252,7 @@ def run_ours(args, dist, rank, world):
     if rank == 0:
         e2e = _e2e(sa, pre, dec, dev, stream, args)
     peaks, peak_src = _peaks()
+    large = _large_configs(sa, dev, stream, flush, peaks, peak_src) if rank == 0 else None
     next_rows = _next_rows(sa, dev, stream, flush, peaks, peak_src) if rank == 0 else None
 
     if rank != 0:
@@ -281,6 +286,8 @@ def run_ours(args, dist, rank, world):
                      "kernel": "prefill_kernel",
                      "peak_source": f"{peak_src} (cuBLAS bf16 burst)"},
         "e2e": e2e,
+        "long_decode": large["long_decode"],
+        "ragged_prefill": large["ragged_prefill"],
         "next_rows": next_rows,
         "cpu_baseline": cpu,
         "gpu_launches": 3 * args.steps,
@@ -322,6 +329,56 @@ def _time_calls(fn, stream, flush=None, steps=20, warmup=3, prepare=None):
         b.record(stream)
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def _large_configs(sa, dev, stream, flush, peaks, peak_src):
+    """The two largest workloads, timed per call after the hot-path region:
+    the long decode (128 sequences of 16384..32768 cached tokens, chunks
+    chosen per length: chunk kernel + merge) against HBM, and the ragged
+    16-sequence prefill (215586 packed tokens) against the bf16 tensor peak."""
+    res = {}
+    ld = workloads.workload("long_decode", device=dev)
+    out = torch.empty(ld.q.shape, dtype=torch.bfloat16, device=dev)
+    need = sa.sink_attn_decode_workspace_bytes(ld.batch, ld.max_seqlen, ld.num_q_heads, ld.num_kv_heads, 64, 16,
+                                               ld.num_splits)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def call_ld():
+        sa.sink_attn_decode(ld.q, ld.k_pages, ld.v_pages, ld.page_table, ld.seqlens_t, ld.sinks, ld.scale,
+                            num_splits=ld.num_splits, out=out, max_seqlen=ld.max_seqlen, workspace=ws)
+
+    ms = _time_calls(call_ld, stream)  # 6.4 GB of K/V: far larger than L2, no flush needed
+    nb = workloads.decode_bytes(ld.seqlens, ld.num_q_heads, ld.num_kv_heads, out_bytes=2)
+    gbs = nb / (ms * 1e-3) / 1e9
+    res["long_decode"] = {
+        "workload": workloads.WORKLOADS["long_decode"], "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 4),
+        "bytes_per_launch": nb, "kernels": "decode_split_kernel + decode_merge_kernel",
+        "chunks": sa.sink_attn_decode_max_splits(ld.batch, ld.max_seqlen, ld.num_kv_heads, 16, ld.num_splits),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "traffic": _traffic("decode_split_kernel/long_decode", DECODE_SOURCES),
+                     "peak_source": f"{peak_src} (STREAM-style copy)"}}
+    del ld, out, ws
+    torch.cuda.empty_cache()
+    rp = workloads.workload("ragged_prefill", device=dev)
+    out = torch.empty(rp.q.shape, dtype=torch.bfloat16, device=dev)
+
+    def call_rp():
+        sa.sink_attn_prefill(rp.q, rp.k, rp.v, rp.sinks, rp.cu_seqlens, rp.scale, out=out, max_seqlen=rp.max_seqlen)
+
+    ms = _time_calls(call_rp, stream, steps=10, flush=flush)
+    fl = workloads.prefill_flops(rp.seqlens, rp.num_q_heads)
+    tf = fl / (ms * 1e-3) / 1e12
+    res["ragged_prefill"] = {
+        "workload": workloads.WORKLOADS["ragged_prefill"], "value": round(tf, 3), "unit": "TFLOP/s",
+        "ms": round(ms, 4), "flops_per_launch": fl, "kernels": "prefill_kernel",
+        "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "traffic": _traffic("prefill_kernel/ragged_prefill", PREFILL_SOURCES),
+                     "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
+    del rp, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def _next_rows(sa, dev, stream, flush, peaks, peak_src):
@@ -541,18 +598,43 @@ def _oracle_decode_sample(dec, seqs=8):
                                       out_bytes=2)
 
 
+def _oracle_large_samples():
+    """The oracle on samples of the two largest workloads: 4 sequences of the
+    long decode (their own lengths), and kv head 0 (8 query heads) of one
+    3314-token sequence of the ragged prefill."""
+    import oracle
+    lens = workloads.workload_seqlens("long_decode")[:4]
+    ld = workloads.make_decode(lens, seed=3, sink_mode="normal2", scale=0.125)
+    t0 = time.perf_counter()
+    oracle.decode(ld.q, ld.k_pages, ld.v_pages, ld.page_table, ld.seqlens_t, ld.sinks, ld.scale)
+    dt = time.perf_counter() - t0
+    nb = workloads.decode_bytes(lens, 64, 8, out_bytes=2)
+    L = 3314
+    rp = workloads.make_prefill([L], num_q_heads=8, num_kv_heads=1, seed=4, sink_mode="mixed", scale=0.125)
+    t0 = time.perf_counter()
+    oracle.prefill(rp.q, rp.k, rp.v, rp.sinks, rp.cu_seqlens, rp.scale)
+    pt = time.perf_counter() - t0
+    fl = workloads.prefill_flops([L], 8)
+    return ({"value": round(nb / dt / 1e9, 4), "unit": "GB/s",
+             "sample": f"4 of the 128 sequences ({sum(lens)} tokens, {nb} algorithmic bytes, {dt:.2f} s)"},
+            {"value": round(fl / pt / 1e12, 6), "unit": "TFLOP/s",
+             "sample": f"one kv head (8 query heads) of a {L}-token sequence ({fl:.3e} flop, {pt:.2f} s)"})
+
+
 def _cpu_baseline():
     """The float64 oracle, as it stands, on a bounded sample of the workload."""
     pre = workloads.workload(PREFILL, device="cpu")
     dt, flops = _oracle_prefill_sample(pre)
     dec = workloads.make_decode([8192] * 8, seed=2, sink_mode="normal2", scale=0.125, num_splits=8)
     ddt, dbytes = _oracle_decode_sample(dec)
+    ld, rp = _oracle_large_samples()
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
             "sample": f"prefill of the 8192-token sequence restricted to {PREFILL_SAMPLE_HEADS} of 64 query heads "
                       f"({flops:.3e} algorithmic flop, {dt:.2f} s)",
             "decode": {"value": round(dbytes / ddt / 1e9, 4), "unit": "GB/s",
                        "sample": f"8 sequences x 8192 tokens of the decode batch ({dbytes} algorithmic bytes, "
-                                 f"{ddt:.2f} s)"}}
+                                 f"{ddt:.2f} s)"},
+            "long_decode": ld, "ragged_prefill": rp}
 
 
 def run_reference(args, dist, rank, world):
