@@ -18,11 +18,13 @@ from .binding import (  # noqa: F401
     sink_attn_decode_multi,
     sink_attn_decode_multi_workspace_bytes,
     sink_attn_decode_noalloc,
+    sink_attn_decode_rope,
     sink_attn_decode_workspace_bytes,
     sink_attn_get_device_error,
     sink_attn_prefill,
     sink_attn_prefill_paged,
     sink_attn_prefill_paged_workspace_bytes,
+    sink_attn_prefill_rope,
     sink_attn_qkv_rope,
     sink_attn_status_string,
     sink_attn_version,

@@ -31,10 +31,13 @@ _SZ = ctypes.c_size_t
 
 EXPORTS = {
     "sink_attn_prefill": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P]),
+    "sink_attn_prefill_rope": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _F, _P, _I, _P, _P]),
     "sink_attn_decode": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                               _P, _SZ, _P]),
     "sink_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P,
                                       _P]),
+    "sink_attn_decode_rope": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _P, _F, _P, _I,
+                                   _P, _P, _SZ, _P]),
     "sink_attn_decode_multi": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I, _P, _I,
                                     _P, _P, _SZ, _P]),
     "sink_attn_prefill_paged": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _I, _I, _I, _I, _F, _I,
@@ -196,6 +199,46 @@ def sink_attn_prefill(q, k, v, sinks, cu_seqlens, scale: float, out=None, out_dt
     return out
 
 
+def sink_attn_prefill_rope(q, k, v, sinks, cu_seqlens, scale: float, inv_freq, attn_factor: float = 1.0,
+                           q_bias=None, out=None, out_dtype=torch.float32, lse=None,
+                           max_seqlen: Optional[int] = None, stream=None):
+    """sink_attn_prefill with the query's bias and rotary encoding applied in
+    the kernel: q [T,Hq,64] bf16 is the raw projection, token i of a sequence
+    at position i; k and v are ready (sink_attn_qkv_rope with q=None).
+    inv_freq [32] fp64 (CUDA), q_bias [Hq,64] bf16 or None.  Returns out."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(sinks, "sinks", torch.float32, 1)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(inv_freq, "inv_freq", torch.float64, 1)
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    if k.shape != (T, hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [T, Hkv, D] with the same T and D as q")
+    if sinks.shape[0] != hq or inv_freq.shape[0] != d // 2:
+        raise ValueError("sinks [Hq] and inv_freq [D/2]")
+    if q_bias is not None:
+        _need(q_bias, "q_bias", torch.bfloat16, 2)
+        if tuple(q_bias.shape) != (hq, d):
+            raise ValueError("q_bias must be [Hq, D]")
+    B = cu_seqlens.shape[0] - 1
+    if max_seqlen is None:
+        max_seqlen = T
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=out_dtype, device=q.device)
+    _check_outputs(out, lse, (T, hq, d), (T, hq))
+    _same_device(q, k=k, v=v, sinks=sinks, cu_seqlens=cu_seqlens, out=out, lse=lse, inv_freq=inv_freq,
+                 q_bias=q_bias)
+    st = load().sink_attn_prefill_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), B, T,
+                                       int(max_seqlen), hq, hkv, d, float(scale), _ptr(q_bias), _ptr(inv_freq),
+                                       float(attn_factor), _ptr(out),
+                                       OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse),
+                                       _stream_ptr(stream))
+    _check(st, "sink_attn_prefill_rope")
+    return out
+
+
 def sink_attn_decode_workspace_bytes(batch: int, max_seqlen: int, num_q_heads: int, num_kv_heads: int,
                                      head_dim: int = 64, page_size: int = 16, num_splits: int = 0) -> int:
     n = load().sink_attn_decode_workspace_bytes(batch, max_seqlen, num_q_heads, num_kv_heads, head_dim,
@@ -259,6 +302,53 @@ def sink_attn_decode(q, k_pages, v_pages, page_table, seqlens, sinks, scale: flo
                                  OUT_F32 if out.dtype == torch.float32 else OUT_BF16, _ptr(lse), ws_ptr,
                                  ws_bytes, _stream_ptr(stream))
     _check(st, "sink_attn_decode")
+    return out
+
+
+def sink_attn_decode_rope(q, k_pages, v_pages, page_table, seqlens, sinks, scale: float, inv_freq,
+                          attn_factor: float = 1.0, q_bias=None, num_splits: int = 0, out=None,
+                          out_dtype=torch.float32, lse=None, max_seqlen: Optional[int] = None, workspace=None,
+                          stream=None):
+    """sink_attn_decode with the query's bias and rotary encoding applied in the
+    kernel: q [B,Hq,64] bf16 is the raw projection; the query of sequence b is
+    rotated by position seqlens[b] - 1.  inv_freq [32] fp64 (CUDA), q_bias
+    [Hq,64] bf16 or None.  The cache holds rotated keys (sink_attn_qkv_rope
+    with q=None).  Returns out [B,Hq,64]."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    _need(sinks, "sinks", torch.float32, 1)
+    _need(inv_freq, "inv_freq", torch.float64, 1)
+    B, hq, d = q.shape
+    if inv_freq.shape[0] != d // 2:
+        raise ValueError("inv_freq must have head_dim / 2 entries")
+    if q_bias is not None:
+        _need(q_bias, "q_bias", torch.bfloat16, 2)
+        if tuple(q_bias.shape) != (hq, d):
+            raise ValueError("q_bias must be [Hq, D]")
+    num_pages, hkv, page_size, _ = k_pages.shape
+    _check_paged(q, k_pages, v_pages, page_table, seqlens, sinks, B, hq, d)
+    if max_seqlen is None:  # the page-table width bounds every length: no device read
+        max_seqlen = page_table.shape[1] * page_size
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    _check_outputs(out, lse, (B, hq, d), (B, hq))
+    _same_device(q, k_pages=k_pages, v_pages=v_pages, page_table=page_table, seqlens=seqlens, sinks=sinks,
+                 out=out, lse=lse, workspace=workspace, inv_freq=inv_freq, q_bias=q_bias)
+    if workspace is None:
+        workspace = _workspace(load().sink_attn_decode_workspace_bytes(B, int(max_seqlen), hq, hkv, d, page_size,
+                                                                       int(num_splits)), q.device, stream)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = load().sink_attn_decode_rope(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), page_table.shape[1],
+                                      _ptr(seqlens), B, int(max_seqlen), num_pages, _ptr(sinks), hq, hkv, d,
+                                      page_size, float(scale), int(num_splits), _ptr(q_bias), _ptr(inv_freq),
+                                      float(attn_factor), _ptr(out), OUT_F32 if out.dtype == torch.float32 else OUT_BF16,
+                                      _ptr(lse), ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check(st, "sink_attn_decode_rope")
     return out
 
 
@@ -381,10 +471,12 @@ def sink_attn_qkv_rope(q, k, v, positions, inv_freq, attn_factor: float = 1.0, q
                        v_bias=None, slot_mapping=None, k_pages=None, v_pages=None, stream=None):
     """In place: q <- rot(q + q_bias), k <- rot(k + k_bias), v <- v + v_bias,
     rotation by positions[t] * inv_freq (half-split planes) times attn_factor.
-    q [T,Hq,64], k/v [T,Hkv,64] bf16; biases [H,64] bf16 or None; positions [T]
+    q [T,Hq,64] (or None: left to sink_attn_prefill_rope / sink_attn_decode_rope),
+    k/v [T,Hkv,64] bf16; biases [H,64] bf16 or None; positions [T]
     int32; inv_freq [32] fp64 (CUDA).  With slot_mapping [T] int32 the new k/v
     are also written to k_pages/v_pages [num_pages,Hkv,16,64] at those slots."""
-    _need(q, "q", torch.bfloat16, 3)
+    if q is not None:
+        _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
     _need(positions, "positions", torch.int32, 1)
@@ -392,10 +484,13 @@ def sink_attn_qkv_rope(q, k, v, positions, inv_freq, attn_factor: float = 1.0, q
     for name, b in (("q_bias", q_bias), ("k_bias", k_bias), ("v_bias", v_bias)):
         if b is not None:
             _need(b, name, torch.bfloat16, 2)
-    T, hq, d = q.shape
-    hkv = k.shape[1]
-    if k.shape != v.shape or k.shape[0] != T or positions.shape[0] != T or inv_freq.shape[0] != d // 2:
+    T, hkv, d = k.shape
+    hq = q.shape[1] if q is not None else (q_bias.shape[0] if q_bias is not None else hkv)
+    if (q is not None and (q.shape[0] != T or q.shape[2] != d)) or k.shape != v.shape or positions.shape[0] != T \
+            or inv_freq.shape[0] != d // 2:
         raise ValueError("q [T,Hq,D], k and v [T,Hkv,D], positions [T], inv_freq [D/2]")
+    _same_device(k, q=q, v=v, positions=positions, inv_freq=inv_freq, q_bias=q_bias, k_bias=k_bias, v_bias=v_bias,
+                 slot_mapping=slot_mapping, k_pages=k_pages, v_pages=v_pages)
     num_pages, page_size = 0, 16
     if slot_mapping is not None:
         _need(slot_mapping, "slot_mapping", torch.int32, 1)

@@ -247,13 +247,20 @@ int prefill_paged_impl(const void* q, const void* k_pages, const void* v_pages, 
                        int num_q_heads, int num_kv_heads, int head_dim, int page_size, float scale, void* out,
                        int out_dtype, float* lse, void* stream);
 
-// Shared body of sink_attn_decode (q_len = 1), sink_attn_decode_multi and
-// sink_attn_prefill_paged.
+// Rotary encoding of q applied inside the decode chunk kernel.
+struct RopeQ {
+  const void* q_bias;
+  const double* inv_freq;
+  float attn_factor;
+};
+
+// Shared body of sink_attn_decode (q_len = 1), sink_attn_decode_rope,
+// sink_attn_decode_multi and sink_attn_prefill_paged.
 int decode_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
                 int page_table_stride, const int32_t* seqlens, int batch, const QueryLayout& ql, int max_seqlen,
                 int num_pages, const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
                 float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
-                size_t workspace_bytes, void* stream);
+                size_t workspace_bytes, void* stream, const RopeQ* rope = nullptr);
 
 }  // namespace
 }  // namespace sa
@@ -340,6 +347,19 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages, co
                      workspace, workspace_bytes, stream);
 }
 
+int sink_attn_decode_rope(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                          int page_table_stride, const int32_t* seqlens, int batch, int max_seqlen, int num_pages,
+                          const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                          float scale, int num_splits, const void* q_bias, const double* inv_freq,
+                          float attn_factor, void* out, int out_dtype, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  const QueryLayout ql{nullptr, 1, batch, 1};
+  const RopeQ rope{q_bias, inv_freq, attn_factor};
+  return decode_impl(q, k_pages, v_pages, page_table, page_table_stride, seqlens, batch, ql, max_seqlen, num_pages,
+                     sinks, num_q_heads, num_kv_heads, head_dim, page_size, scale, num_splits, out, out_dtype, lse,
+                     workspace, workspace_bytes, stream, &rope);
+}
+
 int sink_attn_decode_multi(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
                            int page_table_stride, const int32_t* seqlens, int batch, int q_len, int max_seqlen,
                            int num_pages, const float* sinks, int num_q_heads, int num_kv_heads, int head_dim,
@@ -384,7 +404,7 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
                 int page_table_stride, const int32_t* seqlens, int batch, const QueryLayout& ql, int max_seqlen,
                 int num_pages, const float* sinks, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
                 float scale, int num_splits, void* out, int out_dtype, float* lse, void* workspace,
-                size_t workspace_bytes, void* stream) {
+                size_t workspace_bytes, void* stream, const RopeQ* rope) {
   // ---- validation (nothing is enqueued on failure)
   if (batch < 0 || ql.max_q < 0 || ql.total_q < 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
     return SINK_ATTN_ERR_INVALID_ARG;
@@ -415,6 +435,12 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
     return SINK_ATTN_ERR_INVALID_ARG;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SINK_ATTN_ERR_INVALID_ARG;
   if (workspace && workspace_bytes < pl.ws_bytes) return SINK_ATTN_ERR_INVALID_ARG;
+  if (rope) {
+    if (!rope->inv_freq || !aligned16(rope->inv_freq) || (rope->q_bias && !aligned16(rope->q_bias)))
+      return SINK_ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(rope->attn_factor)) return SINK_ATTN_ERR_INVALID_ARG;
+    if (tensor_cores) return SINK_ATTN_ERR_UNSUPPORTED;  // the rotation lives in the split kernel
+  }
 
   int dev;
   int st = current_device(&dev);
@@ -483,6 +509,11 @@ int decode_impl(const void* q, const void* k_pages, const void* v_pages, const i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.withhold_copies = withhold_copies();
+  if (rope) {
+    p.q_bias = static_cast<const __nv_bfloat16*>(rope->q_bias);
+    p.inv_freq = rope->inv_freq;
+    p.attn_factor = rope->attn_factor;
+  }
   const cudaError_t e = tensor_cores ? launch_decode_tc(qmap, kmap, vmap, p, s) : launch_decode(p, s);
   if (owned) cudaFreeAsync(ws, s);
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
@@ -526,8 +557,8 @@ int sink_attn_qkv_rope(void* q, void* k, void* v, const void* q_bias, const void
   if (!std::isfinite(attn_factor)) return SINK_ATTN_ERR_INVALID_ARG;
   if (head_dim != kHeadDim) return SINK_ATTN_ERR_UNSUPPORTED;
   if (num_tokens == 0) return SINK_ATTN_OK;
-  if (!q || !k || !v || !positions || !inv_freq) return SINK_ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(positions) || !aligned16(inv_freq) ||
+  if (!k || !v || !positions || !inv_freq) return SINK_ATTN_ERR_INVALID_ARG;
+  if ((q && !aligned16(q)) || !aligned16(k) || !aligned16(v) || !aligned16(positions) || !aligned16(inv_freq) ||
       (q_bias && !aligned16(q_bias)) || (k_bias && !aligned16(k_bias)) || (v_bias && !aligned16(v_bias)))
     return SINK_ATTN_ERR_INVALID_ARG;
   if (slot_mapping) {
@@ -628,14 +659,12 @@ int prefill_paged_impl(const void* q, const void* k_pages, const void* v_pages, 
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }
 
-}  // namespace
-}  // namespace sa
 
-extern "C" {
-
-int sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks, const int32_t* cu_seqlens,
-                      int batch, int total_tokens, int max_seqlen, int num_q_heads, int num_kv_heads,
-                      int head_dim, float scale, void* out, int out_dtype, float* lse, void* stream) {
+// Shared body of sink_attn_prefill and sink_attn_prefill_rope (rope: the
+// query rotation inside the kernel, or null).
+int prefill_impl(const void* q, const void* k, const void* v, const float* sinks, const int32_t* cu_seqlens,
+                 int batch, int total_tokens, int max_seqlen, int num_q_heads, int num_kv_heads, int head_dim,
+                 float scale, void* out, int out_dtype, float* lse, void* stream, const RopeQ* rope) {
   if (batch < 0 || total_tokens < 0 || max_seqlen < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
     return SINK_ATTN_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads) return SINK_ATTN_ERR_INVALID_ARG;
@@ -643,6 +672,9 @@ int sink_attn_prefill(const void* q, const void* k, const void* v, const float* 
   if (!(scale > 0.f) || !std::isfinite(scale)) return SINK_ATTN_ERR_INVALID_ARG;
   if (head_dim != kHeadDim) return SINK_ATTN_ERR_UNSUPPORTED;
   if (max_seqlen > total_tokens) return SINK_ATTN_ERR_INVALID_ARG;
+  if (rope && (!rope->inv_freq || !aligned16(rope->inv_freq) || (rope->q_bias && !aligned16(rope->q_bias)) ||
+               !std::isfinite(rope->attn_factor)))
+    return SINK_ATTN_ERR_INVALID_ARG;
   if (batch == 0 || total_tokens == 0) return SINK_ATTN_OK;
   if (!q || !k || !v || !sinks || !cu_seqlens || !out) return SINK_ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(sinks) || !aligned16(cu_seqlens) ||
@@ -686,8 +718,34 @@ int sink_attn_prefill(const void* q, const void* k, const void* v, const float* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_limit_ns = wait_limit_ns();
   p.withhold_copies = withhold_copies();
+  if (rope) {
+    p.q_bias = static_cast<const __nv_bfloat16*>(rope->q_bias);
+    p.inv_freq = rope->inv_freq;
+    p.attn_factor = rope->attn_factor;
+  }
   cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" {
+
+int sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks, const int32_t* cu_seqlens,
+                      int batch, int total_tokens, int max_seqlen, int num_q_heads, int num_kv_heads,
+                      int head_dim, float scale, void* out, int out_dtype, float* lse, void* stream) {
+  return prefill_impl(q, k, v, sinks, cu_seqlens, batch, total_tokens, max_seqlen, num_q_heads, num_kv_heads,
+                      head_dim, scale, out, out_dtype, lse, stream, nullptr);
+}
+
+int sink_attn_prefill_rope(const void* q, const void* k, const void* v, const float* sinks,
+                           const int32_t* cu_seqlens, int batch, int total_tokens, int max_seqlen, int num_q_heads,
+                           int num_kv_heads, int head_dim, float scale, const void* q_bias, const double* inv_freq,
+                           float attn_factor, void* out, int out_dtype, float* lse, void* stream) {
+  const RopeQ rope{q_bias, inv_freq, attn_factor};
+  return prefill_impl(q, k, v, sinks, cu_seqlens, batch, total_tokens, max_seqlen, num_q_heads, num_kv_heads,
+                      head_dim, scale, out, out_dtype, lse, stream, &rope);
 }
 
 }  // extern "C"

@@ -35,6 +35,7 @@
 // shared load below is free of bank conflicts.
 #include "common.cuh"
 #include "decode.h"
+#include "rope.h"
 
 namespace sa {
 
@@ -71,6 +72,52 @@ __device__ __forceinline__ void chunk_range(const DecodeParams& p, int L, int s,
   pg1 = min(npages, pg0 + chunk);
 }
 
+// Sixteen dims [16qd, 16qd+16) of the query row (new token t, head h) as packed
+// bf16 pairs.  With the rotary encoding on, the row's bias is added and the
+// dims rotated against their plane partners (dim i pairs with i +- 32, the
+// other half of the row), with the same roundings as the rotary pass.
+__device__ __forceinline__ void load_query16(const DecodeParams& p, int b, int t, int h, int qd,
+                                             const float2 (&rope_cs)[16][kD / 2], uint32_t (&w)[8]) {
+  const uint4* qr = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.q_len + t) * p.hq + h) * kD);
+  const uint4 lo = __ldg(qr + 2 * qd), hi = __ldg(qr + 2 * qd + 1);
+  const uint32_t own[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  if (!p.inv_freq) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = own[e];
+    return;
+  }
+  const int pq = qd ^ 2;  // the 16 partner dims: the same planes in the other half
+  const uint4 plo = __ldg(qr + 2 * pq), phi = __ldg(qr + 2 * pq + 1);
+  const uint32_t par[8] = {plo.x, plo.y, plo.z, plo.w, phi.x, phi.y, phi.z, phi.w};
+  uint32_t bo[8] = {}, bp[8] = {};
+  if (p.q_bias) {
+    const uint4* br = reinterpret_cast<const uint4*>(p.q_bias + (size_t)h * kD);
+    const uint4 b0 = __ldg(br + 2 * qd), b1 = __ldg(br + 2 * qd + 1);
+    const uint4 c0 = __ldg(br + 2 * pq), c1 = __ldg(br + 2 * pq + 1);
+    const uint32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const uint32_t cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      bo[e] = bb[e];
+      bp[e] = cc[e];
+    }
+  }
+  const bool first_half = qd < 2;
+  const int plane0 = (16 * qd) & (kD / 2 - 1);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float y[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float x = __fadd_rn(k ? bf16x2_hi(own[e]) : bf16x2_lo(own[e]), k ? bf16x2_hi(bo[e]) : bf16x2_lo(bo[e]));
+      const float xp = __fadd_rn(k ? bf16x2_hi(par[e]) : bf16x2_lo(par[e]), k ? bf16x2_hi(bp[e]) : bf16x2_lo(bp[e]));
+      const float2 cs = rope_cs[t][plane0 + 2 * e + k];
+      y[k] = first_half ? rope_first(x, xp, cs.x, cs.y) : rope_second(xp, x, cs.x, cs.y);
+    }
+    w[e] = pack_bf16x2(y[0], y[1]);
+  }
+}
+
 }  // namespace
 
 // Four CTAs per SM (up to 128 registers a thread, so nothing spills), each
@@ -104,22 +151,25 @@ __global__ void __launch_bounds__(kThreads, 4) decode_split_kernel(const DecodeP
   const int lim_r = row_ok ? L - p.q_len + t_r + 1 : L;
   const int lim_r8 = row8_ok ? L - p.q_len + t_r8 + 1 : L;
 
+  // Rotary encoding of q (optional): cos and sin of every (new token, plane),
+  // times the factor, computed once for the CTA (q_len <= 16 tokens here).
+  __shared__ float2 rope_cs[16][kD / 2];
+  if (p.inv_freq) {
+    for (int e = threadIdx.x; e < p.q_len * (kD / 2); e += kThreads) {
+      const int t = e / (kD / 2), i = e % (kD / 2);
+      float c, sn;
+      rope_cos_sin(L - p.q_len + t, rope_turn_increment(__ldg(p.inv_freq + i)), c, sn);
+      rope_cs[t][i] = make_float2(__fmul_rn(c, p.attn_factor), __fmul_rn(sn, p.attn_factor));
+    }
+    __syncthreads();
+  }
+
   // Query fragments: row r holds dims [16qd, 16qd+16) of its head.
   uint32_t qa[4][4];
   {
-    uint4 lo_r = make_uint4(0, 0, 0, 0), hi_r = lo_r, lo_r8 = lo_r, hi_r8 = lo_r;
-    if (row_ok) {
-      const uint4* qr = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.q_len + t_r) * p.hq + h_r) * kD);
-      lo_r = __ldg(qr + 2 * qd);
-      hi_r = __ldg(qr + 2 * qd + 1);
-    }
-    if (row8_ok) {
-      const uint4* qr = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.q_len + t_r8) * p.hq + h_r8) * kD);
-      lo_r8 = __ldg(qr + 2 * qd);
-      hi_r8 = __ldg(qr + 2 * qd + 1);
-    }
-    const uint32_t wr[8] = {lo_r.x, lo_r.y, lo_r.z, lo_r.w, hi_r.x, hi_r.y, hi_r.z, hi_r.w};
-    const uint32_t wr8[8] = {lo_r8.x, lo_r8.y, lo_r8.z, lo_r8.w, hi_r8.x, hi_r8.y, hi_r8.z, hi_r8.w};
+    uint32_t wr[8] = {}, wr8[8] = {};
+    if (row_ok) load_query16(p, b, t_r, h_r, qd, rope_cs, wr);
+    if (row8_ok) load_query16(p, b, t_r8, h_r8, qd, rope_cs, wr8);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       qa[kk][0] = wr[2 * kk];

@@ -36,6 +36,12 @@ struct DecodeParams {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int withhold_copies;  // failure-path test: the tensor-core kernel's producer issues no copies, so its waits time out
+  // Rotary encoding of q inside the split kernel (null inv_freq: q is used as given).
+  // New token t of a sequence with L cached tokens sits at position L - q_len + t;
+  // its query rows become rot(q + q_bias) * attn_factor, rounded to bf16.
+  const __nv_bfloat16* q_bias;  // [Hq, 64] or null
+  const double* inv_freq;       // [32] radians per position, or null
+  float attn_factor;
 };
 
 // Number of chunks sequence with `npages` pages is cut into.  Every chunk is

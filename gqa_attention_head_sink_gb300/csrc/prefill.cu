@@ -54,6 +54,7 @@
 // on another sequence's values.
 #include "common.cuh"
 #include "prefill.h"
+#include "rope.h"
 #include "tcgen05.cuh"
 
 #include <algorithm>
@@ -82,11 +83,18 @@ constexpr float kRescaleThreshold = 8.f;
 constexpr int kOffQ = 0;                                // 2 Q tiles
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;         // kSlots K/V tiles
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;  // mbarriers
-constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
+constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2;
 constexpr int kOffMisc = kOffBar + 256;
 constexpr int kOffSeq = kOffMisc + 64;
 constexpr int kSeqArrays = 6;
 constexpr int kSmemBytes = kOffSeq + kSeqArrays * kPrefillMaxBatch * 4 + 1024;
+// Rotary mode adds a table of cos/sin(r * f_i) for the 128 rows of a query
+// tile and the 32 planes ([plane][row] float2: conflict-free row reads), and
+// the planes' fixed-point turn increments.
+constexpr int kOffRopeLo = kOffSeq + kSeqArrays * kPrefillMaxBatch * 4;
+constexpr int kOffRopeTurn = kOffRopeLo + 32 * kTile * 8;
+constexpr int kSmemBytesRope = kOffRopeTurn + 32 * 8 + 1024;
+static_assert(kSmemBytesRope <= 227 * 1024, "shared memory of the rotary mode");
 constexpr int kPage = 16;
 constexpr int kSlabBytes = kPage * kD * 2;  // one (page, kv head) slab: 2 KiB
 static_assert(kNumBars * 8 <= 256, "barrier area");
@@ -101,6 +109,7 @@ struct Bars {
   uint64_t* p_full;  // [2] softmax -> MMA: P written (and O rescaled)
   uint64_t* o_done;  // [2] MMA -> softmax: a PV (hence every earlier MMA) finished
   uint64_t* drain;
+  uint64_t* q_ready;  // [2] rotary mode, softmax -> MMA: the unit's Q tile of the head is rotated
 };
 
 // Walks the longest-first list of query blocks.  Level n holds the query
@@ -155,6 +164,55 @@ __device__ __forceinline__ int paged_kend(int kv_len, int q_len, int qb) {
   return kv_len - q_len + min(q_len, (qb + 1) * kTile);
 }
 
+// Rotary encoding of query row r of a Q tile in shared memory (128-byte swizzle:
+// 16-byte chunk c of row r at chunk c ^ (r % 8)), in place.  Row r is token
+// qb * 128 + r of its sequence, at that position: cos/sin of the position's
+// multiple of 128 come from lane `plane` of the warp (ch, sh), those of r from
+// the table lo[plane * 128 + r]; the angles are added, the bias added and the
+// plane rotated exactly as the rotary pass does it (rope.h), then rounded to bf16.
+__device__ __forceinline__ void rope_q_row(uint8_t* tile, int r, const __nv_bfloat16* bias_row, float ch, float sh,
+                                           const float2* lo, float af) {
+  uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
+  const uint4* b4 = reinterpret_cast<const uint4*>(bias_row);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // chunk c holds dims 8c..8c+7, chunk c + 4 their plane partners
+    const uint4 v1 = row[c ^ (r & 7)], v2 = row[(c + 4) ^ (r & 7)];
+    const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w}, w2[4] = {v2.x, v2.y, v2.z, v2.w};
+    uint32_t b1[4] = {0, 0, 0, 0}, b2[4] = {0, 0, 0, 0};
+    if (bias_row) {
+      const uint4 u1 = __ldg(b4 + c), u2 = __ldg(b4 + c + 4);
+      b1[0] = u1.x; b1[1] = u1.y; b1[2] = u1.z; b1[3] = u1.w;
+      b2[0] = u2.x; b2[1] = u2.y; b2[2] = u2.z; b2[3] = u2.w;
+    }
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float y1[2], y2[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int plane = 8 * c + 2 * e + k;
+        float x1 = k ? bf16x2_hi(w1[e]) : bf16x2_lo(w1[e]);
+        float x2 = k ? bf16x2_hi(w2[e]) : bf16x2_lo(w2[e]);
+        if (bias_row) {
+          x1 = __fadd_rn(x1, k ? bf16x2_hi(b1[e]) : bf16x2_lo(b1[e]));
+          x2 = __fadd_rn(x2, k ? bf16x2_hi(b2[e]) : bf16x2_lo(b2[e]));
+        }
+        const float chp = __shfl_sync(0xffffffffu, ch, plane), shp = __shfl_sync(0xffffffffu, sh, plane);
+        const float2 l = lo[plane * kTile + r];
+        float cc, sn;
+        rope_angle_add(chp, shp, l.x, l.y, cc, sn);
+        const float cs = __fmul_rn(cc, af), ss = __fmul_rn(sn, af);
+        y1[k] = rope_first(x1, x2, cs, ss);
+        y2[k] = rope_second(x1, x2, cs, ss);
+      }
+      o1[e] = pack_bf16x2(y1[0], y1[1]);
+      o2[e] = pack_bf16x2(y2[0], y2[1]);
+    }
+    row[c ^ (r & 7)] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    row[(c + 4) ^ (r & 7)] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  }
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const PrefillParams& p,
                                               volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;  // fast path: already complete
@@ -166,7 +224,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 
 }  // namespace
 
-template <bool kPaged>
+template <bool kPaged, bool kRopeQ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -183,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.p_full = bars.s_free + 2;
   bars.o_done = bars.p_full + 2;
   bars.drain = bars.o_done + 2;
+  bars.q_ready = bars.drain + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* total_qblocks = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -195,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* tmp_nqb = seq_nqb + kPrefillMaxBatch;                  // by batch index
   int* seq_kv = tmp_nqb + kPrefillMaxBatch;                   // sorted; paged mode: cached tokens
   int* seq_id = seq_kv + kPrefillMaxBatch;                    // sorted; paged mode: batch index
+  float2* rope_lo = reinterpret_cast<float2*>(smem + kOffRopeLo);                    // rotary mode
+  unsigned long long* rope_turn = reinterpret_cast<unsigned long long*>(smem + kOffRopeTurn);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.batch;
@@ -204,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int len = max(0, __ldg(p.cu_seqlens + i + 1) - __ldg(p.cu_seqlens + i));
     tmp_nqb[i] = (len + kTile - 1) / kTile;
   }
+  if (kRopeQ && tid < 32) rope_turn[tid] = rope_turn_increment(__ldg(p.inv_freq + tid));
   if (tid == 0) {
     mbar_init(bars.q_full, 1);
     mbar_init(bars.q_empty, 2);  // released by both MMA warps
@@ -218,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.o_done + t, 1);
     }
     mbar_init(bars.drain, 2);
+    mbar_init(bars.q_ready, 128);
+    mbar_init(bars.q_ready + 1, 128);
     *abort_flag = 0;
     *zeroed_count = 0;
     fence_barrier_init();
@@ -228,6 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
   }
   __syncthreads();
+  if constexpr (kRopeQ) {  // cos/sin of r * f for the 128 rows of a tile, every plane
+    for (int e = tid; e < 32 * kTile; e += kThreads) {
+      float c, sn;
+      rope_phase_cos_sin(e % kTile, rope_turn[e / kTile], c, sn);
+      rope_lo[e] = make_float2(c, sn);
+    }
+  }
   for (int i = tid; i < B; i += kThreads) {
     const int mine = tmp_nqb[i];
     int rank = 0, total = 0;
@@ -372,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         kend = paged_kend(seq_kv[u.seq], seq_len[u.seq], u.qb);
         n = max(1, (kend + kTile - 1) / kTile);
       }
-      if (!(ok = wait_all(bars.q_full, k & 1))) break;
+      // rotary mode: the softmax warps rotate the landed tile first
+      if (!(ok = wait_all(kRopeQ ? bars.q_ready + t : bars.q_full, k & 1))) break;
       // K_0 -> S (once the softmax has released S)
       if (!(ok = wait_all(bars.slot_full + ring_i % kSlots, (ring_i / kSlots) & 1))) break;
       if (!first_qk) {
@@ -475,9 +547,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     uint32_t sph = 0, oph = 0;
+    // Rotary mode: rotate this thread's row of the head's Q tile of unit kk once it
+    // has landed, then hand the tile to the MMA warp.
+    auto rotate_unit = [&](const Unit& un, int kk) -> bool {
+      if (!__all_sync(0xffffffffu, wait_or_abort(bars.q_full, kk & 1, p, abort_flag))) return false;
+      const int hA = un.g * p.group + 2 * un.pair;
+      const int hT = (t && 2 * un.pair + 1 < p.group) ? hA + 1 : hA;  // the head the producer loaded
+      float ch, sh;
+      rope_phase_cos_sin(un.qb * kTile, rope_turn[lane], ch, sh);
+      rope_q_row(q_tile[t], r, p.q_bias ? p.q_bias + (size_t)hT * kD : nullptr, ch, sh, rope_lo, p.attn_factor);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
+      mbar_arrive(bars.q_ready + t);
+      return true;
+    };
     Unit u;
     bool ok = true;
     for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+      if constexpr (kRopeQ) {
+        if (k == 0 && !(ok = rotate_unit(u, 0))) break;
+      }
       int n = u.qb + 1;
       int lim0 = 0;     // paged mode: keys visible to this row, counted from the unit's first key tile
       int j_mask = 0;   // paged mode: first key tile that crosses the last key of some row of this warp
@@ -571,6 +659,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
         tc_fence_before();
         mbar_arrive(bars.p_full + t);
+        if constexpr (kRopeQ) {
+          // the next unit's tile has landed by now (loaded after this unit's last QK):
+          // rotate it while this unit's last PV runs
+          Unit un;
+          if (j == n - 1 && next_unit(k + 1, total_units, pairs_per_group, p.hkv, cur, un) &&
+              !(ok = rotate_unit(un, k + 1)))
+            break;
+        }
       }
       if (!ok) break;
       // ---- epilogue: wait for the last PV, normalise, store
@@ -620,9 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 cudaError_t prefill_configure() {
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = cudaFuncSetAttribute(prefill_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytesRope);
 }
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -631,9 +731,11 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, con
   const long long upper = ppg * p.hkv * ((long long)(p.total_tokens + kTile - 1) / kTile + p.batch);
   const int grid = (int)std::min<long long>(std::max(1, num_sms), std::max(1LL, upper));
   if (paged)
-    prefill_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+    prefill_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  else if (p.inv_freq)
+    prefill_kernel<false, true><<<grid, kThreads, kSmemBytesRope, stream>>>(qmap, kmap, vmap, p);
   else
-    prefill_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+    prefill_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -31,6 +32,12 @@ struct PrefillParams {
   const int32_t* kv_len;      // [B]
   const int32_t* page_table;  // [B, stride]
   int stride;
+  // Rotary mode (contiguous prefill only; null inv_freq: off): q is the raw
+  // projection, and row i of a sequence becomes rot(q + q_bias) * attn_factor
+  // at position i, rotated in shared memory before its first QK.
+  const __nv_bfloat16* q_bias;  // [Hq, 64] or null
+  const double* inv_freq;       // [32]
+  float attn_factor;
 };
 
 // One-time per-device kernel attributes (dynamic shared memory size).

@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(kThreads) qkv_rope_kernel(const RopeParams p) 
     if (t < p.tokens) {
       float s, c;
       rope_cos_sin(__ldg(p.positions + t), turn[i], c, s);
-      cs[tb][i] = c * p.attn_factor;
-      sn[tb][i] = s * p.attn_factor;
+      cs[tb][i] = __fmul_rn(c, p.attn_factor);
+      sn[tb][i] = __fmul_rn(s, p.attn_factor);
     }
     if (i == 0) {
       // cache slot of this token's k and v: row of the [num_pages * Hkv * page_size, 64] view (kv head 0)
@@ -86,16 +86,18 @@ __global__ void __launch_bounds__(kThreads) qkv_rope_kernel(const RopeParams p) 
   }
   __syncthreads();
 
-  // q and k rows: items (token, head, lane); heads 0..Hq-1 are q, then k
-  const int rows = p.hq + p.hkv;
+  // q and k rows: items (token, head, lane); heads 0..Hq-1 are q (none when q is
+  // left alone), then k
+  const int q_rows = p.q ? p.hq : 0;
+  const int rows = q_rows + p.hkv;
   const int qk_items = kTokensPerBlock * rows * kLanesPerRow;
   for (int item = tid; item < qk_items; item += kThreads) {
     const int tb = item / (rows * kLanesPerRow), rest = item % (rows * kLanesPerRow);
     const int h = rest / kLanesPerRow, l = rest % kLanesPerRow;
     const int t = t_base + tb;
     if (t >= p.tokens) break;  // items are token-major: the rest are past the end too
-    const bool is_q = h < p.hq;
-    const int hh = is_q ? h : h - p.hq;
+    const bool is_q = h < q_rows;
+    const int hh = is_q ? h : h - q_rows;
     __nv_bfloat16* row = is_q ? p.q + ((size_t)t * p.hq + hh) * kD : p.k + ((size_t)t * p.hkv + hh) * kD;
     const __nv_bfloat16* bias = is_q ? p.q_bias : p.k_bias;
     float x1[8], x2[8];
@@ -107,16 +109,16 @@ __global__ void __launch_bounds__(kThreads) qkv_rope_kernel(const RopeParams p) 
       unpack8(__ldg(reinterpret_cast<const uint4*>(bias + (size_t)hh * kD + kHalf + 8 * l)), b2);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        x1[e] += b1[e];
-        x2[e] += b2[e];
+        x1[e] = __fadd_rn(x1[e], b1[e]);
+        x2[e] = __fadd_rn(x2[e], b2[e]);
       }
     }
     float y1[8], y2[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float c = cs[tb][8 * l + e], s = sn[tb][8 * l + e];
-      y1[e] = x1[e] * c - x2[e] * s;
-      y2[e] = x2[e] * c + x1[e] * s;
+      y1[e] = rope_first(x1[e], x2[e], c, s);
+      y2[e] = rope_second(x1[e], x2[e], c, s);
     }
     const uint4 o1 = pack8(y1), o2 = pack8(y2);
     *reinterpret_cast<uint4*>(row + 8 * l) = o1;

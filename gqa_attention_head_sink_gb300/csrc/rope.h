@@ -8,7 +8,7 @@
 namespace sa {
 
 struct RopeParams {
-  __nv_bfloat16* q;  // [tokens, hq, 64], rotated in place
+  __nv_bfloat16* q;  // [tokens, hq, 64], rotated in place; null: q is left alone
   __nv_bfloat16* k;  // [tokens, hkv, 64], rotated in place
   __nv_bfloat16* v;  // [tokens, hkv, 64], biased in place
   const __nv_bfloat16* q_bias;  // [hq, 64] or null
@@ -38,11 +38,40 @@ __device__ __forceinline__ unsigned long long rope_turn_increment(double f) {
   return scaled >= 18446744073709551616.0 ? 0ull : __double2ull_rn(scaled);
 }
 
-// cos and sin of the angle position * f, F = rope_turn_increment(f).
-__device__ __forceinline__ void rope_cos_sin(int position, unsigned long long F, float& c, float& s) {
+// cos and sin of position * f for a position held exactly by the phase.
+__device__ __forceinline__ void rope_phase_cos_sin(int position, unsigned long long F, float& c, float& s) {
   const unsigned long long phase = (unsigned long long)(long long)position * F;  // modulo 2^64 = one turn
   const float half_turns = (float)(int)(phase >> 32) * 0x1p-31f;                 // in [-1, 1)
   sincospif(half_turns, &s, &c);
+}
+
+// Angle addition with every rounding explicit, so that each kernel applying
+// the rotation gets the same bits: (c, s) of a + b from those of a and b.
+__device__ __forceinline__ void rope_angle_add(float ca, float sa, float cb, float sb, float& c, float& s) {
+  c = __fmaf_rn(ca, cb, -__fmul_rn(sa, sb));
+  s = __fmaf_rn(sa, cb, __fmul_rn(ca, sb));
+}
+
+// cos and sin of position * f, F = rope_turn_increment(f).  The position is
+// split into its multiple of 128 and its remainder (both exact phases), the
+// two angles added: a kernel whose 128 consecutive positions share the first
+// part (a prefill query tile) can keep the second part's 128 values in a
+// table and reproduce these bits.
+__device__ __forceinline__ void rope_cos_sin(int position, unsigned long long F, float& c, float& s) {
+  const int lo = position & 127, hi = position - lo;
+  float ch, sh, cl, sl;
+  rope_phase_cos_sin(hi, F, ch, sh);
+  rope_phase_cos_sin(lo, F, cl, sl);
+  rope_angle_add(ch, sh, cl, sl, c, s);
+}
+
+// The rotation of one plane (x1 = dim i, x2 = dim i + D/2) by cs = c * factor,
+// sn = s * factor, with explicit roundings (identical wherever it is used).
+__device__ __forceinline__ float rope_first(float x1, float x2, float cs, float sn) {
+  return __fmaf_rn(x1, cs, -__fmul_rn(x2, sn));
+}
+__device__ __forceinline__ float rope_second(float x1, float x2, float cs, float sn) {
+  return __fmaf_rn(x2, cs, __fmul_rn(x1, sn));
 }
 
 __global__ void qkv_rope_kernel(const RopeParams p);

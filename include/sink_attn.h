@@ -92,6 +92,32 @@ int sink_attn_prefill(const void* q, const void* k, const void* v, const float* 
                       void* out, int out_dtype, float* lse, void* stream);
 
 /*
+ * sink_attn_prefill with the query's bias and rotary position encoding applied
+ * inside the prefill kernel ("GPT-OSS on day 0": model overview, YaRN
+ * positional encoding and biased QKV projections; section Sink Attention for
+ * the attention).  Each 128-row query tile is rotated in shared memory after
+ * it lands and before its first score product, so the rotated query never
+ * goes through HBM.
+ *
+ * q is the query projection before its bias and rotation; k and v are ready
+ * (biased and rotated k, biased v: sink_attn_qkv_rope with q = NULL).  Token
+ * i of a sequence (0-based within it) is at position i, so its query rows
+ * become rot(q + q_bias) * attn_factor at position i, computed exactly as
+ * sink_attn_qkv_rope computes them at that position (same bits) and rounded
+ * to bf16 before the attention: the output equals that of sink_attn_qkv_rope
+ * followed by sink_attn_prefill, bit for bit.
+ *   q_bias      bf16 [num_q_heads, head_dim] DEVICE, or NULL for no bias
+ *   inv_freq    fp64 [head_dim / 2] DEVICE, radians per position
+ *   attn_factor YaRN's temperature, 1 for plain RoPE
+ * Every other argument, limit and result is that of sink_attn_prefill.
+ */
+int sink_attn_prefill_rope(const void* q, const void* k, const void* v, const float* sinks,
+                           const int32_t* cu_seqlens, int batch, int total_tokens, int max_seqlen,
+                           int num_q_heads, int num_kv_heads, int head_dim, float scale,
+                           const void* q_bias, const double* inv_freq, float attn_factor,
+                           void* out, int out_dtype, float* lse, void* stream);
+
+/*
  * Split-KV decode: one query token per sequence against a paged KV cache
  * ("GPT-OSS on day 0", section Sink Attention: the key length is split into
  * chunks and only the first chunk's online state starts from the sink).
@@ -133,6 +159,34 @@ int sink_attn_decode(const void* q, const void* k_pages, const void* v_pages,
                      int page_size, float scale, int num_splits,
                      void* out, int out_dtype, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * sink_attn_decode with the query's bias and rotary position encoding applied
+ * inside the decode kernel, so the query of a decode step needs no separate
+ * pass ("GPT-OSS on day 0": model overview, YaRN positional encoding and
+ * biased QKV projections; section Sink Attention for the attention).
+ *
+ * q is the query projection before its bias and rotation.  The keys and
+ * values in the cache are already biased and rotated (sink_attn_qkv_rope with
+ * q = NULL appends the step's k and v that way).  The query of sequence b is
+ * the last of its seqlens[b] cached tokens, so it is rotated by position
+ * seqlens[b] - 1: every query row becomes rot(q + q_bias) * attn_factor,
+ * computed exactly as sink_attn_qkv_rope computes it (same bits) and rounded
+ * to bf16 before the attention.
+ *   q_bias      bf16 [num_q_heads, head_dim] DEVICE, or NULL for no bias
+ *   inv_freq    fp64 [head_dim / 2] DEVICE, radians per position
+ *               (sink_attn_yarn_inv_freq)
+ *   attn_factor YaRN's temperature, 1 for plain RoPE
+ * Every other argument, limit and result is that of sink_attn_decode.
+ */
+int sink_attn_decode_rope(const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* page_table, int page_table_stride,
+                          const int32_t* seqlens, int batch, int max_seqlen, int num_pages,
+                          const float* sinks, int num_q_heads, int num_kv_heads, int head_dim,
+                          int page_size, float scale, int num_splits,
+                          const void* q_bias, const double* inv_freq, float attn_factor,
+                          void* out, int out_dtype, float* lse,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of workspace sink_attn_decode needs for these arguments (0 when no
@@ -305,7 +359,10 @@ int sink_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_p
  * result is rounded once to bf16.
  *
  *   q, k, v     bf16 [num_tokens, H, head_dim] (H = num_q_heads for q,
- *               num_kv_heads for k and v), DEVICE, modified in place
+ *               num_kv_heads for k and v), DEVICE, modified in place.  q may
+ *               be NULL: only k and v are processed, for attention calls
+ *               that rotate q themselves (sink_attn_prefill_rope,
+ *               sink_attn_decode_rope).
  *   q_bias, k_bias, v_bias
  *               bf16 [H, head_dim] DEVICE, or NULL for no bias
  *   positions   int32 [num_tokens] DEVICE: position of each token in its

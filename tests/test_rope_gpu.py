@@ -20,7 +20,7 @@ import torch
 import gqa_attention_head_sink_gb300 as sa
 import oracle
 from gqa_attention_head_sink_gb300 import build, workloads
-from tests.parity import assert_parity, bf16_spacing, to_f64
+from tests.parity import assert_parity, bf16_spacing, lse_close, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -117,3 +117,73 @@ def test_bias_rope_then_prefill_matches_oracle():
     out = sa.sink_attn_prefill(d.q, d.k, d.v, d.sinks, d.cu_seqlens, d.scale, max_seqlen=max(lens))
     torch.cuda.synchronize()
     assert_parity(out, want)
+
+
+@pytest.mark.parametrize("lens,hq,hkv,splits,yarn,with_bias", [
+    ([500, 77, 1, 4096], 64, 8, 8, (150000.0, 32.0, 4096, 32.0, 1.0), True),
+    ([300, 16, 2000], 16, 2, 0, (10000.0, 1.0, 4096, 32.0, 1.0), False),
+    ([8192] * 4, 64, 8, 0, (150000.0, 32.0, 4096, 32.0, 1.0), True),
+])
+def test_decode_rope_fuses_the_query_rotation(lens, hq, hkv, splits, yarn, with_bias):
+    # the query of each sequence is rotated inside the decode kernel by position
+    # seqlens[b] - 1: the same bits as the rotary pass followed by plain decode, and
+    # within tolerance of the oracle's float64 rotation (rounded to bf16) + decode
+    d = workloads.make_decode(lens, num_q_heads=hq, num_kv_heads=hkv, seed=len(lens) + hq, sink_mode="mixed",
+                              num_splits=splits, device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(41)
+    bq = (0.5 * torch.randn(hq, 64, generator=g)).to(torch.bfloat16).cuda() if with_bias else None
+    f, af = sa.sink_attn_yarn_inv_freq(64, *yarn)
+    f = f.cuda()
+    pos = (d.seqlens_t - 1).clamp(min=0)
+    fused = sa.sink_attn_decode_rope(d.q, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale, f, af,
+                                     q_bias=bq, num_splits=splits, max_seqlen=d.max_seqlen)
+    q2 = d.q.clone()
+    dummy = torch.zeros((d.batch, hkv, 64), dtype=torch.bfloat16, device="cuda")
+    sa.sink_attn_qkv_rope(q2, dummy, dummy.clone(), pos, f, af, q_bias=bq)
+    separate = sa.sink_attn_decode(q2, d.k_pages, d.v_pages, d.page_table, d.seqlens_t, d.sinks, d.scale,
+                                   num_splits=splits, max_seqlen=d.max_seqlen)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, separate)
+    f64, af64 = oracle.yarn_inv_freq(64, *yarn)
+    qr, _, _ = oracle.qkv_bias_rope(d.q.cpu(), dummy.cpu(), dummy.cpu(), None if bq is None else bq.cpu(), None,
+                                    None, pos.cpu(), f64, af64)
+    want, _ = oracle.decode(torch.from_numpy(qr).to(torch.bfloat16), d.k_pages.cpu(), d.v_pages.cpu(),
+                            d.page_table.cpu(), d.seqlens_t.cpu(), d.sinks.cpu(), d.scale)
+    assert_parity(fused, want)
+
+
+@pytest.mark.parametrize("lens,hq,hkv,yarn,with_bias", [
+    ([300, 129, 1, 0, 517], 64, 8, (150000.0, 32.0, 4096, 32.0, 1.0), True),
+    ([1000, 128, 256], 16, 2, (10000.0, 1.0, 4096, 32.0, 1.0), False),
+    ([777], 6, 2, (500000.0, 8.0, 8192, 16.0, 2.0), True),  # odd group: a pair's second head is absent
+])
+def test_prefill_rope_fuses_the_query_rotation(lens, hq, hkv, yarn, with_bias):
+    # q is rotated inside the prefill kernel (token i of a sequence at position i): the
+    # same bits as the rotary pass on q followed by plain prefill, and within tolerance
+    # of the oracle's float64 pass (rounded to bf16) + prefill
+    inp = workloads.make_prefill(lens, num_q_heads=hq, num_kv_heads=hkv, seed=sum(lens) % 89, sink_mode="mixed",
+                                 device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(42)
+    r = lambda *shape: (0.5 * torch.randn(*shape, generator=g)).to(torch.bfloat16)  # noqa: E731
+    bq, bk, bv = (r(hq, 64), r(hkv, 64), r(hkv, 64)) if with_bias else (None, None, None)
+    cu = lambda t: None if t is None else t.cuda()  # noqa: E731
+    pos = torch.cat([torch.arange(L, dtype=torch.int32) for L in lens])
+    f, af = sa.sink_attn_yarn_inv_freq(64, *yarn)
+    f = f.cuda()
+    q_raw, k, v = inp.q.clone(), inp.k.clone(), inp.v.clone()
+    sa.sink_attn_qkv_rope(None, k, v, pos.cuda(), f, af, q_bias=cu(bq), k_bias=cu(bk), v_bias=cu(bv))
+    lse = torch.empty((inp.total_tokens, hq), dtype=torch.float32, device="cuda")
+    fused = sa.sink_attn_prefill_rope(q_raw, k, v, inp.sinks, inp.cu_seqlens, inp.scale, f, af, q_bias=cu(bq),
+                                      lse=lse, max_seqlen=inp.max_seqlen)
+    q_rot = q_raw.clone()
+    sa.sink_attn_qkv_rope(q_rot, torch.zeros_like(k), torch.zeros_like(v), pos.cuda(), f, af, q_bias=cu(bq))
+    separate = sa.sink_attn_prefill(q_rot, k, v, inp.sinks, inp.cu_seqlens, inp.scale, max_seqlen=inp.max_seqlen)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, separate)
+    assert torch.equal(q_raw, inp.q)  # the caller's q is not modified
+    f64, af64 = oracle.yarn_inv_freq(64, *yarn)
+    q2, k2, v2 = oracle.qkv_bias_rope(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), bq, bk, bv, pos, f64, af64)
+    rb = lambda x: torch.from_numpy(x).to(torch.bfloat16)  # noqa: E731
+    want, want_lse = oracle.prefill(rb(q2), rb(k2), rb(v2), inp.sinks.cpu(), inp.cu_seqlens.cpu(), inp.scale)
+    assert_parity(fused, want)
+    lse_close(lse, want_lse)
