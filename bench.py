@@ -387,27 +387,31 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
     (tensor bound) and the QKV bias + YaRN rotary pass (HBM bound).  Timed
     per call (chunk kernel + merge kernel where there is one)."""
     res = {}
-    mtp = workloads.workload("mtp_decode", device=dev)
-    out = torch.empty(mtp.q.shape, dtype=torch.bfloat16, device=dev)
-    need = sa.sink_attn_decode_multi_workspace_bytes(mtp.batch, mtp.q_len, mtp.max_seqlen, mtp.num_q_heads,
-                                                     mtp.num_kv_heads, 64, 16, mtp.num_splits)
-    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    for q_len in (4, 8, 16):
+        mtp = workloads.workload("mtp_decode", device=dev, q_len=q_len)
+        out = torch.empty(mtp.q.shape, dtype=torch.bfloat16, device=dev)
+        need = sa.sink_attn_decode_multi_workspace_bytes(mtp.batch, mtp.q_len, mtp.max_seqlen, mtp.num_q_heads,
+                                                         mtp.num_kv_heads, 64, 16, mtp.num_splits)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
-    def call_mtp():
-        sa.sink_attn_decode_multi(mtp.q, mtp.k_pages, mtp.v_pages, mtp.page_table, mtp.seqlens_t, mtp.sinks,
-                                  mtp.scale, num_splits=mtp.num_splits, out=out, max_seqlen=mtp.max_seqlen,
-                                  workspace=ws)
+        def call_mtp():
+            sa.sink_attn_decode_multi(mtp.q, mtp.k_pages, mtp.v_pages, mtp.page_table, mtp.seqlens_t, mtp.sinks,
+                                      mtp.scale, num_splits=mtp.num_splits, out=out, max_seqlen=mtp.max_seqlen,
+                                      workspace=ws)
 
-    ms = _time_calls(call_mtp, stream)  # 1 GiB of K/V: larger than L2, no flush needed
-    nb = workloads.decode_bytes(mtp.seqlens, mtp.num_q_heads, mtp.num_kv_heads, out_bytes=2, q_len=mtp.q_len)
-    gbs = nb / (ms * 1e-3) / 1e9
-    res["multi_token_decode"] = {
-        "workload": workloads.WORKLOADS["mtp_decode"], "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 4),
-        "bytes_per_launch": nb, "kernels": "decode_tc_kernel + decode_merge_kernel",
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "traffic": _traffic("decode_tc_kernel/mtp_decode", DECODE_TC_SOURCES),
-                     "peak_source": f"{peak_src} (STREAM-style copy)"}}
+        ms = _time_calls(call_mtp, stream)  # 1 GiB of K/V: larger than L2, no flush needed
+        nb = workloads.decode_bytes(mtp.seqlens, mtp.num_q_heads, mtp.num_kv_heads, out_bytes=2, q_len=mtp.q_len)
+        gbs = nb / (ms * 1e-3) / 1e9
+        key = "multi_token_decode" if q_len == 4 else f"multi_token_decode_q{q_len}"
+        res[key] = {
+            "workload": workloads.WORKLOADS["mtp_decode"].replace("the last 4 of them new (4 queries",
+                                                                  f"the last {q_len} of them new ({q_len} queries"),
+            "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 4), "bytes_per_launch": nb,
+            "kernels": "decode_tc_kernel + decode_merge_kernel",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": _traffic(f"decode_tc_kernel/mtp_decode_q{q_len}", DECODE_TC_SOURCES),
+                         "peak_source": f"{peak_src} (STREAM-style copy)"}}
     del mtp, out, ws
     cp = workloads.workload("chunked_prefill", device=dev)
     out = torch.empty(cp.q.shape, dtype=torch.bfloat16, device=dev)

@@ -33,11 +33,18 @@ constexpr int kMaxGroupDecode = 16;
 constexpr int kTensorCoreMinRows = 17;
 constexpr int kMaxDecodeTokens = 4096;  // new tokens per sequence in one decode call
 constexpr int kMaxDevices = 64;
-// Chunk sizing for num_splits == 0: aim for about this many CTAs in the
-// chunk grid (8 per SM of a 152-SM GB300) with 16..128 pages per chunk.
+// Chunk sizing for num_splits == 0.  The split kernel (four small CTAs per
+// SM) aims at about this many CTAs in the chunk grid (8 per SM of a 152-SM
+// GB300) with 16..128 pages per chunk.
 constexpr long long kDecodeTargetCtas = 152 * 8;
 constexpr int kMinSplitPages = 16;
 constexpr int kMaxSplitPages = 128;
+// The tensor-core kernel (two large CTAs per SM, each paying a Q load and a
+// first-tile latency of ~2.5 us before its first tile) aims at about 1.5
+// waves of its CTAs, with chunks as long as that allows: at batch 64 x 8192
+// one chunk per sequence (512 CTAs) ran at 85-90 % of the HBM copy figure for
+// 4..16 new tokens, four chunks at 69-86 %.
+constexpr long long kDecodeTcTargetCtas = 152 * 3;
 
 std::mutex g_mutex;
 unsigned* g_err_ptr[kMaxDevices] = {};
@@ -210,10 +217,10 @@ bool plan_decode(int batch, int max_q, long long total_q, int max_seqlen, int nu
   if (num_splits > 0) {
     max_splits = (int)std::max(1LL, std::min<long long>(num_splits, max_pages));
   } else {
-    long long sp = ((long long)batch * row_tiles * num_kv_heads * max_pages + kDecodeTargetCtas - 1) /
-                   kDecodeTargetCtas;
+    const long long target = tensor_cores ? kDecodeTcTargetCtas : kDecodeTargetCtas;
+    long long sp = ((long long)batch * row_tiles * num_kv_heads * max_pages + target - 1) / target;
     sp = std::max<long long>(kMinSplitPages, sp);
-    if (row_tiles == 1) sp = std::min<long long>(kMaxSplitPages, sp);
+    if (row_tiles == 1 && !tensor_cores) sp = std::min<long long>(kMaxSplitPages, sp);
     if ((max_pages + sp - 1) / sp > kMaxSplits) sp = (max_pages + kMaxSplits - 1) / kMaxSplits;
     split_pages = (int)sp;
     max_splits = (int)std::max(1LL, (max_pages + sp - 1) / sp);
