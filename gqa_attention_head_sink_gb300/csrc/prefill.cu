@@ -9,10 +9,10 @@
 // Design (persistent, warp-specialised, one CTA per SM):
 //   * work unit = (sequence, 128-row query block, pair of query heads of one
 //     GQA group).  The two heads share every K/V tile, so a tile is staged once
-//     for two 128x128 score tiles.  Units are ordered longest first (query
-//     blocks with the most key tiles first), the heads of one group adjacent so
-//     that concurrently running CTAs read the same K/V from L2, and dealt to
-//     CTAs in a serpentine order.
+//     for two 128x128 score tiles.  Units are ordered by sequence (longest
+//     first) and within a sequence by query block (most key tiles first), the
+//     heads of one group adjacent, so that concurrently running CTAs read the
+//     same K/V from L2; they are dealt to CTAs in a serpentine order.
 //   * warp 2 (elected lane): TMA producer.  Loads the two 128x64 Q tiles of a
 //     unit, then K_0, V_0, K_1, V_1, ... through an 8-slot ring of 16 KiB
 //     tiles (128-byte swizzle), each slot guarded by a full/empty mbarrier.
@@ -112,30 +112,30 @@ struct Bars {
   uint64_t* q_ready;  // [2] rotary mode, softmax -> MMA: the unit's Q tile of the head is rotated
 };
 
-// Walks the longest-first list of query blocks.  Level n holds the query
-// block n-1 of every sequence with at least n blocks; sequences are sorted by
-// block count, so level n's sequences are the first cnt(n) of the sorted list.
+// Walks the list of query blocks in schedule order: sequences longest first,
+// and within a sequence its query blocks from the last (most key tiles) to the
+// first.  Consecutive blocks, which concurrently running CTAs take, then read
+// the same sequence's keys and values, so those stay in L2 (level by level
+// across all sequences, the keys of every long sequence were live at once and
+// re-read from HBM).  Sequences are sorted by block count.
 struct Cursor {
   const int* nqb;  // sorted, descending
   int batch;
-  int level, cnt, start;
+  int seq, start;  // current sequence (sorted index) and its first block's index
   __device__ void init(const int* nqb_sorted, int b) {
     nqb = nqb_sorted;
     batch = b;
-    level = b > 0 ? nqb[0] : 0;
-    cnt = 0;
-    while (cnt < batch && nqb[cnt] >= level) ++cnt;
+    seq = 0;
     start = 0;
   }
   // qbl must not decrease between calls.  Returns the sorted sequence index.
   __device__ int seek(int qbl, int& qb) {
-    while (qbl >= start + cnt) {
-      start += cnt;
-      --level;
-      while (cnt < batch && nqb[cnt] >= level) ++cnt;
+    while (seq < batch - 1 && qbl >= start + nqb[seq]) {
+      start += nqb[seq];
+      ++seq;
     }
-    qb = level - 1;
-    return qbl - start;
+    qb = nqb[seq] - 1 - (qbl - start);
+    return seq;
   }
 };
 
@@ -659,16 +659,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
         tc_fence_before();
         mbar_arrive(bars.p_full + t);
-        if constexpr (kRopeQ) {
-          // the next unit's tile has landed by now (loaded after this unit's last QK):
-          // rotate it while this unit's last PV runs
-          Unit un;
-          if (j == n - 1 && next_unit(k + 1, total_units, pairs_per_group, p.hkv, cur, un) &&
-              !(ok = rotate_unit(un, k + 1)))
-            break;
-        }
       }
       if (!ok) break;
+      if constexpr (kRopeQ) {
+        // rotate the next unit's tile (loaded once this unit's last QK was issued) while
+        // this unit's last PV runs; kept out of the tile loop, whose every iteration ran
+        // slower with it inside
+        Unit un;
+        if (next_unit(k + 1, total_units, pairs_per_group, p.hkv, cur, un) && !(ok = rotate_unit(un, k + 1))) break;
+      }
       // ---- epilogue: wait for the last PV, normalise, store
       ok = wait_or_abort(bars.o_done + t, oph, p, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
