@@ -457,7 +457,38 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": _traffic("qkv_rope_kernel", ROPE_SOURCES),
                      "peak_source": f"{peak_src} (STREAM-style copy)"}}
-    del ro, pristine
+    # The same 8192 raw projections through attention, two ways: the query's
+    # bias and rotation inside the prefill kernel (the pass then handles k and
+    # v only), against the full pass followed by the plain prefill.
+    sinks = (2.0 * torch.randn(64, generator=torch.Generator(device=dev).manual_seed(1), device=dev)).float()
+    cu = torch.tensor([0, 8192], dtype=torch.int32, device=dev)
+    out = torch.empty(ro.q.shape, dtype=torch.bfloat16, device=dev)
+
+    def call_fused():
+        sa.sink_attn_qkv_rope(None, ro.k, ro.v, ro.positions, f, af, None, ro.k_bias, ro.v_bias)
+        sa.sink_attn_prefill_rope(ro.q, ro.k, ro.v, sinks, cu, 0.125, f, af, q_bias=ro.q_bias, out=out,
+                                  max_seqlen=8192)
+
+    def call_separate():
+        sa.sink_attn_qkv_rope(ro.q, ro.k, ro.v, ro.positions, f, af, ro.q_bias, ro.k_bias, ro.v_bias)
+        sa.sink_attn_prefill(ro.q, ro.k, ro.v, sinks, cu, 0.125, out=out, max_seqlen=8192)
+
+    ms_fused = _time_calls(call_fused, stream, flush=flush, prepare=restore)
+    ms_sep = _time_calls(call_separate, stream, flush=flush, prepare=restore)
+    fl = workloads.prefill_flops([8192], 64)
+    tf = fl / (ms_fused * 1e-3) / 1e12
+    res["rope_prefill"] = {
+        "workload": "the 8192-token rotary workload's raw q/k/v (positions 0..8191, YaRN and biases as qkv_rope) "
+                    "through the gpt-oss prefill (one sequence, causal, Hq=64, Hkv=8, D=64, sinks 2*N(0,1), "
+                    "scale 1/8)",
+        "value": round(tf, 3), "unit": "TFLOP/s", "ms": round(ms_fused, 4), "flops_per_launch": fl,
+        "kernels": "qkv_rope_kernel (k and v) + prefill_kernel, rotary mode (query rotated in shared memory)",
+        "separate": {"value": round(fl / (ms_sep * 1e-3) / 1e12, 3), "ms": round(ms_sep, 4),
+                     "kernels": "qkv_rope_kernel (q, k and v) + prefill_kernel"},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(tf / peaks["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
+    del ro, pristine, out
     torch.cuda.empty_cache()
     return res
 
