@@ -407,7 +407,8 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
             "workload": workloads.WORKLOADS["mtp_decode"].replace("the last 4 of them new (4 queries",
                                                                   f"the last {q_len} of them new ({q_len} queries"),
             "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 4), "bytes_per_launch": nb,
-            "kernels": "decode_tc_kernel + decode_merge_kernel",
+            "kernels": ("decode_tc_kernel + decode_merge_kernel" if need > 0
+                        else "decode_tc_kernel (one chunk per sequence, written directly: no merge)"),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": _traffic(f"decode_tc_kernel/mtp_decode_q{q_len}", DECODE_TC_SOURCES),

@@ -1,14 +1,13 @@
 """GPU parity of split-KV paged decode against the float64 oracle.
 
 All calls go through the C ABI (ctypes binding).  Small cases are compared on
-every element; the full-size workloads (batch 64 x 8192 tokens with 8 chunks,
-the launch the benchmark times, and batch 128 x 16K-32K tokens with chunks
-chosen per length) are compared on sampled sequences (every head, every
-dimension), which the oracle evaluates one by one.
+every element; so are the full-size workloads (batch 64 x 8192 tokens with 8
+chunks, the launch the benchmark times, and batch 128 x 16K-32K tokens with
+chunks chosen per length): every sequence, head and dimension, the mean error
+taken over the whole output.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -152,22 +151,20 @@ def test_decode_rejects_bad_shapes():
 def test_decode_full_batch64_len8192_splits8():
     inp = workloads.workload("decode", device="cuda")
     out, lse = run(inp, with_lse=True)
-    seqs = [0, 1, 31, 62, 63]
-    want, want_lse = oracle_decode(inp, seqs)
-    assert_parity(out[seqs], want)
-    lse_close(lse[seqs], want_lse)
+    want, want_lse = oracle_decode(inp)  # all 64 sequences
+    assert_parity(out, want)
+    lse_close(lse, want_lse)
     out_bf, _ = run(inp, out_dtype=torch.bfloat16)
-    assert_parity(out_bf[seqs], want, bf16_output=True)
+    assert_parity(out_bf, want, bf16_output=True)
 
 
 @pytest.mark.slow
 def test_decode_full_batch128_long_auto_splits():
     inp = workloads.workload("long_decode", device="cuda")
-    out, _ = run(inp)
-    lens = np.array(inp.seqlens)
-    seqs = sorted({int(lens.argmin()), int(lens.argmax()), 0, 64, 127})
-    want, _ = oracle_decode(inp, seqs)
-    assert_parity(out[seqs], want)
+    out, lse = run(inp, with_lse=True)
+    want, want_lse = oracle_decode(inp)  # all 128 sequences
+    assert_parity(out, want)
+    lse_close(lse, want_lse)
 
 
 @pytest.mark.slow

@@ -140,17 +140,19 @@ def test_decode_multi_rejects_too_many_tokens():
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("q_len", [2, 4, 8, 16])
-def test_decode_multi_full_size_sampled(q_len):
-    # batch 64 x 8192 cached tokens, 8 chunks: the shape of the decode benchmark
-    inp = workloads.make_decode([8192] * 64, seed=2, sink_mode="normal2", num_splits=8, q_len=q_len,
-                                device="cuda")
+@pytest.mark.parametrize("q_len,splits", [(2, 8), (4, 0), (8, 0), (16, 0), (16, 8)])
+def test_decode_multi_full_size(q_len, splits):
+    # batch 64 x 8192 cached tokens: with chunks chosen per length (0) exactly the launch the
+    # benchmark times, and with 8 chunks merged; every sequence, head and element compared
+    if splits == 0:
+        inp = workloads.workload("mtp_decode", device="cuda", q_len=q_len)
+    else:
+        inp = workloads.make_decode([8192] * 64, seed=2, sink_mode="normal2", num_splits=splits, q_len=q_len,
+                                    device="cuda")
     out, lse = run(inp, out_dtype=torch.bfloat16, with_lse=True)
-    seqs = [0, 37, 63]
-    want, want_lse = oracle_multi(inp, seqs)
-    assert_parity(out[seqs], want, bf16_output=True)
-    lse_close(lse[seqs], want_lse)
-    assert torch.isfinite(out.float()).all()
+    want, want_lse = oracle_multi(inp)
+    assert_parity(out, want, bf16_output=True)
+    lse_close(lse, want_lse)
 
 
 @pytest.mark.parametrize("q_len", [2, 8])  # the split kernel, then the tensor-core kernel
