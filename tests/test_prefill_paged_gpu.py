@@ -9,16 +9,16 @@ t sees keys 0 .. L_b - n_b + t.  Cases: prefixes of every length including
 none (plain causal prefill) and sequences with no new token, more new tokens
 than cached ones, groups 1 to 16, forced and automatic chunking of the key
 length, ragged page tails with poisoned slots, and at full size 8192 new
-tokens after an 8192-token prefix, checked on sampled rows (each one a
-single-query decode over the keys it sees).  All calls go through the C ABI.
+tokens after an 8192-token prefix (the benchmark's workload), checked on
+every element.  All calls go through the C ABI.
 """
-import numpy as np
 import pytest
 import torch
 
 import gqa_attention_head_sink_gb300 as sa
 import oracle
 from gqa_attention_head_sink_gb300 import build, workloads
+from tests.full_parity import check_paged_prefill_everywhere
 from tests.parity import assert_parity, lse_close
 
 pytestmark = pytest.mark.gpu
@@ -112,20 +112,15 @@ def test_prefill_paged_splits_agree():
         assert_parity(out, want)
 
 
-def test_prefill_paged_full_size_sampled():
-    # 8192 new tokens after an 8192-token prefix (Hq 64, Hkv 8): no key split
+def test_prefill_paged_full_size():
+    # 8192 new tokens after an 8192-token prefix (Hq 64, Hkv 8): the benchmark's launch (keys not
+    # split, the prefill kernel's paged mode); every element of the bf16 output and the lse
     L, n = 16384, 8192
-    inp = workloads.make_paged_prefill([L], [n], seed=53, sink_mode="normal2", num_splits=0, device="cuda")
+    inp = workloads.workload("chunked_prefill", device="cuda")
+    assert inp.seqlens == [L] and inp.q_lens == [n]
     out, lse = run(inp, out_dtype=torch.bfloat16, with_lse=True)
-    assert torch.isfinite(out.float()).all()
-    rows = [0, 1, 15, 16, 127, 128, 4095, 6000, n - 2, n - 1]
-    kp, vp = inp.k_pages.cpu(), inp.v_pages.cpu()
-    q = inp.q.cpu()
-    for t in rows:  # token t sees the first L - n + t + 1 keys: a single-query decode over them
-        want, want_lse = oracle.decode(q[t][None], kp, vp, inp.page_table.cpu(),
-                                       torch.tensor([L - n + t + 1], dtype=torch.int32), inp.sinks.cpu(), inp.scale)
-        assert_parity(out[t][None], want, bf16_output=True)
-        lse_close(lse[t][None], want_lse)
+    total = check_paged_prefill_everywhere(inp, out16=out, lse=lse)
+    assert total["out16"]["n"] == n * inp.num_q_heads * 64
 
 
 @pytest.mark.parametrize("n_new", [700, 90])  # the prefill kernel's paged mode, then the tensor-core decode kernel
