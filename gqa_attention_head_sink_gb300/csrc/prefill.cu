@@ -462,6 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n == 1) umma_commit(bars.q_empty);
       }
       ++ring_i;
+      // keys of the unit's last tile it needs (only the last tile can end early)
+      const int valid_last = (kPaged ? kend : seq_len[u.seq]) - (n - 1) * kTile;
       for (int j = 0; j < n; ++j) {
         const uint32_t vi = ring_i, ki = ring_i + 1;
         const bool more = j + 1 < n;
@@ -487,8 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // keys of this tile the unit needs: paged mode, up to its last row's position;
           // contiguous mode, up to the sequence end (only the last query block's
           // diagonal tile can end early, when the length is not a multiple of 128)
-          const int valid = (kPaged ? kend : seq_len[u.seq]) - j * kTile;
-          if (valid < kTile) {
+          const int valid = valid_last;
+          if (j == n - 1 && valid < kTile) {
             // rows past them (slabs not copied, slots past the sequence end, or the next
             // packed sequence's tokens) enter the product with weight 0, and 0 x NaN is NaN:
             // head 0's warp zeroes them (fence for the tensor core's reads); head 1's waits.
