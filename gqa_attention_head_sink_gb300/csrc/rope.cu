@@ -11,13 +11,16 @@
 // frequencies themselves are a per-model table computed once on the host
 // (sink_attn_yarn_inv_freq in api.cu).
 //
-// Why a separate pass and not inside the attention kernels' tile loads: each
-// K tile is read by every query block of its sequence (64 times at 8192
+// Why K is rotated here and not at the attention kernels' tile loads: each K
+// tile is read by every query block of its sequence (64 times at 8192
 // tokens), so rotating at load would repeat the work 64 times on the softmax
-// warps that already bound the prefill; one bandwidth-bound pass over q, k
-// and v costs ~5 % of the prefill's time instead.  For decode and chunked
-// prefill the same pass writes the new tokens' rotated k and v into their
-// cache slots, so the attention kernels read the cache unchanged.
+// warps that already bound the prefill.  q may be left out (q == NULL): the
+// prefill and decode kernels can rotate each query tile once themselves
+// (their rotary mode, bit for bit the same as this pass); on the 8192-token
+// prefill this pass over q, k and v plus the plain prefill is the faster
+// route.  For decode and chunked prefill the same pass writes the new
+// tokens' rotated k and v into their cache slots, so the attention kernels
+// read the cache unchanged.
 //
 // One CTA per 8 tokens: each thread first forms one (token, plane) entry of
 // the cos/sin table (the angle position * inv_freq as a 64-bit fixed-point
