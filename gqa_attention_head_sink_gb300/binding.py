@@ -489,6 +489,11 @@ def sink_attn_qkv_rope(q, k, v, positions, inv_freq, attn_factor: float = 1.0, q
     if (q is not None and (q.shape[0] != T or q.shape[2] != d)) or k.shape != v.shape or positions.shape[0] != T \
             or inv_freq.shape[0] != d // 2:
         raise ValueError("q [T,Hq,D], k and v [T,Hkv,D], positions [T], inv_freq [D/2]")
+    # the kernel reads a bias row per head and writes cache slots per kv head: smaller buffers
+    # would be read or written past their ends on the device
+    for name, b, h in (("q_bias", q_bias, hq), ("k_bias", k_bias, hkv), ("v_bias", v_bias, hkv)):
+        if b is not None and tuple(b.shape) != (h, d):
+            raise ValueError(f"{name} must be [{h}, {d}], got {tuple(b.shape)}")
     _same_device(k, q=q, v=v, positions=positions, inv_freq=inv_freq, q_bias=q_bias, k_bias=k_bias, v_bias=v_bias,
                  slot_mapping=slot_mapping, k_pages=k_pages, v_pages=v_pages)
     num_pages, page_size = 0, 16
@@ -497,6 +502,10 @@ def sink_attn_qkv_rope(q, k, v, positions, inv_freq, attn_factor: float = 1.0, q
         _need(k_pages, "k_pages", torch.bfloat16, 4)
         _need(v_pages, "v_pages", torch.bfloat16, 4)
         num_pages, page_size = k_pages.shape[0], k_pages.shape[2]
+        if slot_mapping.shape[0] != T:
+            raise ValueError("slot_mapping needs one slot per token")
+        if v_pages.shape != k_pages.shape or k_pages.shape[1] != hkv or k_pages.shape[3] != d:
+            raise ValueError("k_pages and v_pages must both be [num_pages, Hkv, page_size, D] with the Hkv and D of k")
     st = load().sink_attn_qkv_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(q_bias), _ptr(k_bias), _ptr(v_bias),
                                    _ptr(positions), _ptr(inv_freq), float(attn_factor), T, hq, hkv, d,
                                    _ptr(slot_mapping), _ptr(k_pages), _ptr(v_pages), num_pages, page_size,

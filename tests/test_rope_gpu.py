@@ -96,6 +96,33 @@ def test_qkv_rope_appends_to_the_paged_cache():
     assert bool((kp.permute(0, 2, 1, 3)[untouched] == 7.0).all()) and bool((vp.permute(0, 2, 1, 3)[untouched] == 7.0).all())
 
 
+def test_qkv_rope_rejects_buffers_it_would_overrun():
+    # a bias with fewer heads, a slot mapping shorter than the tokens, or cache pools with
+    # fewer kv heads would be read or written past their ends: refused before any launch
+    T, hq, hkv = 16, 8, 2
+    q, k, v, (bq, bk, bv) = _inputs(T, hq, hkv, seed=9)
+    q, k, v, bq, bk, bv = (t.cuda() for t in (q, k, v, bq, bk, bv))
+    pos = torch.arange(T, dtype=torch.int32, device="cuda")
+    f, af = sa.sink_attn_yarn_inv_freq(64)
+    f = f.cuda()
+    kp = torch.zeros((4, hkv, 16, 64), dtype=torch.bfloat16, device="cuda")
+    slots = torch.arange(T, dtype=torch.int32, device="cuda")
+    bad = [
+        dict(q_bias=bq[:4]),
+        dict(k_bias=bk[:1]),
+        dict(v_bias=bv[:, :32].contiguous()),
+        dict(slot_mapping=slots[:8], k_pages=kp, v_pages=kp.clone()),
+        dict(slot_mapping=slots, k_pages=kp[:, :1].contiguous(), v_pages=kp[:, :1].contiguous()),
+        dict(slot_mapping=slots, k_pages=kp, v_pages=kp[:2].contiguous()),
+    ]
+    before = (q.clone(), k.clone(), v.clone())
+    for kw in bad:
+        with pytest.raises(ValueError):
+            sa.sink_attn_qkv_rope(q, k, v, pos, f, af, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(q, before[0]) and torch.equal(k, before[1]) and torch.equal(v, before[2])
+
+
 def test_bias_rope_then_prefill_matches_oracle():
     lens = [300, 129]
     inp = workloads.make_prefill(lens, seed=7, sink_mode="normal2")
