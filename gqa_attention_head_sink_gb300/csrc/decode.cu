@@ -421,44 +421,74 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
   } else {
     b = row / p.q_len;
   }
-  const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
-  int n, pg0, pg1;
-  chunk_range(p, L, 0, n, pg0, pg1);
   const size_t slot0 = (size_t)wid * p.max_splits;
   const float2* md = reinterpret_cast<const float2*>(p.ws_md) + slot0;  // (m_c, d_c)
-  float M = -INFINITY;
-  for (int c = lane; c < n; c += 32) M = fmaxf(M, md[c].x);
+  const float2* o = reinterpret_cast<const float2*>(p.ws_o + slot0 * kD) + lane;  // chunk c at o[c * 32]
+  float W = 0.f, a0 = 0.f, a1 = 0.f, M = -INFINITY;
+  if (p.max_splits <= 16) {
+    // Up to 16 chunks: every load of the row at once, before the length that says how
+    // many of them this sequence used (slots past that count hold another call's
+    // values and are skipped, never multiplied by a zero weight): one round trip to
+    // L2 instead of three (3.6 against 5.7 us for the batch-64 decode's merge).
+    float2 oc[16];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float W = 0.f, a0 = 0.f, a1 = 0.f;
-  if (M != -INFINITY) {
-    const float2* o = reinterpret_cast<const float2*>(p.ws_o + slot0 * kD) + lane;  // chunk c at o[c * 32]
-    for (int base = 0; base < n; base += 32) {
-      // chunk base + lane's weight on this lane; the dims loop reads it by shuffle
-      float f = 0.f;
-      if (base + lane < n) {
-        const float2 v = md[base + lane];
-        f = fast_exp2(v.x - M);  // 0 for a chunk that saw nothing
-        W += v.y * f;
-      }
-      const int cnt = min(32, n - base);
-      for (int k = 0; k < cnt; k += 8) {  // eight chunks' loads in flight before their adds
-        float2 oc[8];
-        float fk[8];
+    for (int u = 0; u < 16; ++u) oc[u] = u < p.max_splits ? o[(size_t)u * 32] : make_float2(0.f, 0.f);
+    const float2 v = lane < p.max_splits ? md[lane] : make_float2(-INFINITY, 0.f);
+    const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
+    int n, pg0, pg1;
+    chunk_range(p, L, 0, n, pg0, pg1);
+    M = lane < n ? v.x : -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          fk[u] = __shfl_sync(0xffffffffu, f, k + u);
-          oc[u] = k + u < cnt ? o[(size_t)(base + k + u) * 32] : make_float2(0.f, 0.f);
-        }
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (M != -INFINITY) {
+      const float f = lane < n ? fast_exp2(v.x - M) : 0.f;  // 0 for a chunk that saw nothing
+      W = lane < n ? v.y * f : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          a0 += oc[u].x * fk[u];
-          a1 += oc[u].y * fk[u];
+      for (int u = 0; u < 16; ++u) {
+        const float fu = __shfl_sync(0xffffffffu, f, u);
+        if (u < n) {
+          a0 += oc[u].x * fu;
+          a1 += oc[u].y * fu;
         }
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
     }
+  } else {
+    const int L = min(max(0, p.seqlens[b]), p.stride * kPage);
+    int n, pg0, pg1;
+    chunk_range(p, L, 0, n, pg0, pg1);
+    for (int c = lane; c < n; c += 32) M = fmaxf(M, md[c].x);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (M != -INFINITY) {
+      for (int base = 0; base < n; base += 32) {
+        // chunk base + lane's weight on this lane; the dims loop reads it by shuffle
+        float f = 0.f;
+        if (base + lane < n) {
+          const float2 v = md[base + lane];
+          f = fast_exp2(v.x - M);  // 0 for a chunk that saw nothing
+          W += v.y * f;
+        }
+        const int cnt = min(32, n - base);
+        for (int k = 0; k < cnt; k += 8) {  // eight chunks' loads in flight before their adds
+          float2 oc[8];
+          float fk[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            fk[u] = __shfl_sync(0xffffffffu, f, k + u);
+            oc[u] = k + u < cnt ? o[(size_t)(base + k + u) * 32] : make_float2(0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            a0 += oc[u].x * fk[u];
+            a1 += oc[u].y * fk[u];
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    }
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   const size_t o_off = (size_t)wid * kD + 2 * lane;
