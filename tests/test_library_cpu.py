@@ -124,6 +124,48 @@ def test_prefill_empty_is_noop(lib):
     assert _prefill_call(lib, total=0, max_seqlen=0) == 0
 
 
+def _prefill_rope_call(lib, inv_freq=8 * 200, q_bias=None, attn_factor=1.0, **kw):
+    args = dict(q=8 * 16, k=8 * 32, v=8 * 48, sinks=8 * 64, cu=8 * 80, batch=2, total=300, max_seqlen=200,
+                hq=8, hkv=2, d=64, scale=0.125, out=8 * 96, out_dtype=1, lse=None)
+    args.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731  (fake, never dereferenced)
+    return lib.sink_attn_prefill_rope(P(args["q"]), P(args["k"]), P(args["v"]), P(args["sinks"]), P(args["cu"]),
+                                      args["batch"], args["total"], args["max_seqlen"], args["hq"], args["hkv"],
+                                      args["d"], args["scale"], P(q_bias), P(inv_freq), attn_factor, P(args["out"]),
+                                      args["out_dtype"], P(args["lse"]), None)
+
+
+def _decode_rope_call(lib, inv_freq=8 * 200, q_bias=None, attn_factor=1.0, **kw):
+    args = dict(q=8 * 16, k=8 * 32, v=8 * 48, table=8 * 64, stride=4, seqlens=8 * 80, batch=2, max_seqlen=64,
+                num_pages=8, sinks=8 * 96, hq=8, hkv=2, d=64, page=16, scale=0.125, splits=0, out=8 * 112,
+                out_dtype=1, lse=None)
+    args.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.sink_attn_decode_rope(P(args["q"]), P(args["k"]), P(args["v"]), P(args["table"]), args["stride"],
+                                     P(args["seqlens"]), args["batch"], args["max_seqlen"], args["num_pages"],
+                                     P(args["sinks"]), args["hq"], args["hkv"], args["d"], args["page"],
+                                     args["scale"], args["splits"], P(q_bias), P(inv_freq), attn_factor,
+                                     P(args["out"]), args["out_dtype"], P(args["lse"]), None, 0, None)
+
+
+@pytest.mark.parametrize("call", [_prefill_rope_call, _decode_rope_call])
+@pytest.mark.parametrize("kw", [
+    dict(inv_freq=None),                  # the frequency table is required
+    dict(inv_freq=8 * 200 + 8),           # misaligned table
+    dict(q_bias=8 * 300 + 2),             # misaligned bias
+    dict(attn_factor=float("inf")),
+    dict(attn_factor=float("nan")),
+    dict(scale=-1.0),
+])
+def test_fused_rotary_calls_reject_bad_arguments_on_host(lib, call, kw):
+    assert call(lib, **kw) == 1  # SINK_ATTN_ERR_INVALID_ARG, nothing enqueued
+
+
+def test_fused_rotary_calls_empty_is_noop(lib):
+    assert _prefill_rope_call(lib, batch=0) == 0
+    assert _decode_rope_call(lib, batch=0) == 0
+
+
 def test_decode_planning(lib):
     # fixed splits: at most one chunk per page
     assert sa.sink_attn_decode_max_splits(64, 8192, 8, 16, 8) == 8
