@@ -662,7 +662,9 @@ int prefill_paged_impl(const void* q, const void* k_pages, const void* v_pages, 
   p.kv_len = seqlens_k;
   p.page_table = page_table;
   p.stride = page_table_stride;
-  cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, true, static_cast<cudaStream_t>(stream));
+  CUtensorMap omap = qmap;
+  if (!p.out_f32 && (st = encode_tokens_heads(&omap, out, total_q, num_q_heads, kPrefillTileRows))) return st;
+  cudaError_t e = launch_prefill(qmap, kmap, vmap, omap, p, sms, true, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }
 
@@ -730,7 +732,9 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* sinks
     p.inv_freq = rope->inv_freq;
     p.attn_factor = rope->attn_factor;
   }
-  cudaError_t e = launch_prefill(qmap, kmap, vmap, p, sms, false, static_cast<cudaStream_t>(stream));
+  CUtensorMap omap = qmap;
+  if (!p.out_f32 && (st = encode_tokens_heads(&omap, out, total_tokens, num_q_heads, kPrefillTileRows))) return st;
+  cudaError_t e = launch_prefill(qmap, kmap, vmap, omap, p, sms, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SINK_ATTN_OK : SINK_ATTN_ERR_CUDA;
 }
 

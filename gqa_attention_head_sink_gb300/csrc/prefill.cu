@@ -26,7 +26,12 @@
 //     (so the MMA for the next key tile overlaps this tile's softmax), applies
 //     the causal mask on the diagonal tile, updates (m, d), and writes P (bf16)
 //     to its own TMEM columns once the previous tile's PV has finished with
-//     them; at the end it normalises O by d and stores the row.
+//     them; at the end it normalises O by d and stores the row.  A bf16 block
+//     whose 128 rows all belong to the sequence goes out through a staging
+//     tile per head (the Q tile's swizzled layout) and one bulk tensor store:
+//     128 threads each storing a 128-byte row 8 KiB away from its neighbours'
+//     held up every unit change by about 2,000 cycles.  Partial blocks and
+//     fp32 output store their rows directly.
 //   * warp 0 allocates / frees the 512 TMEM columns:
 //       S_0 [0,128)  S_1 [128,256)  O_0 [256,320)  O_1 [320,384)  P_0 [384,448)  P_1 [448,512)
 //     P has two bf16 per column.  Keeping P apart from S means a QK MMA never
@@ -83,11 +88,15 @@ constexpr float kRescaleThreshold = 8.f;
 constexpr int kOffQ = 0;                                // 2 Q tiles
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;         // kSlots K/V tiles
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;  // mbarriers
-constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2;
+constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 + 2;
 constexpr int kOffMisc = kOffBar + 256;
 constexpr int kOffSeq = kOffMisc + 64;
 constexpr int kSeqArrays = 6;
-constexpr int kSmemBytes = kOffSeq + kSeqArrays * kPrefillMaxBatch * 4 + 1024;
+// bf16 output of a whole 128-row block leaves through a staging tile per head
+// (the Q tile's layout: 128-byte swizzle) and one bulk tensor store
+constexpr int kOffStage = (kOffSeq + kSeqArrays * kPrefillMaxBatch * 4 + 1023) / 1024 * 1024;
+constexpr int kSmemBytes = kOffStage + 2 * kTileBytes + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // Rotary mode adds a table of cos/sin(r * f_i) for the 128 rows of a query
 // tile and the 32 planes ([plane][row] float2: conflict-free row reads), and
 // the planes' fixed-point turn increments.
@@ -227,7 +236,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 template <bool kPaged, bool kRopeQ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                   const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -242,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.o_done = bars.p_full + 2;
   bars.drain = bars.o_done + 2;
   bars.q_ready = bars.drain + 1;
+  uint64_t* stg_full = bars.q_ready + 2;  // [2] softmax rows of a block written to the staging tile
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* total_qblocks = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -282,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bars.drain, 2);
     mbar_init(bars.q_ready, 128);
     mbar_init(bars.q_ready + 1, 128);
+    mbar_init(stg_full, 128);
+    mbar_init(stg_full + 1, 128);
     *abort_flag = 0;
     *zeroed_count = 0;
     fence_barrier_init();
@@ -435,9 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t), a_p = tmem + col_p(t);
     int zeroings = 0;  // tail-V zeroings met so far
-    Unit u;
+    Unit u, un;
     bool ok = true;
-    for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+    bool have = next_unit(0, total_units, pairs_per_group, p.hkv, cur, u), have_next = false;
+    for (int k = 0; ok && have; ++k, u = un, have = have_next) {
       int n = u.qb + 1, kend = 0;
       if constexpr (kPaged) {
         kend = paged_kend(seq_kv[u.seq], seq_len[u.seq], u.qb);
@@ -461,6 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(bars.slot_empty + ring_i % kSlots);
         if (n == 1) umma_commit(bars.q_empty);
       }
+      // the next unit, worked out here, where the warp has only waits ahead of it
+      have_next = next_unit(k + 1, total_units, pairs_per_group, p.hkv, cur, un);
       ++ring_i;
       // keys of the unit's last tile it needs (only the last tile can end early)
       const int valid_last = (kPaged ? kend : seq_len[u.seq]) - (n - 1) * kTile;
@@ -543,6 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;             // TMEM lane quarter of this warp
     const int r = quad * 32 + lane;        // query row within the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const bool stg_issuer = quad == 0 && lane == 0;  // issues and waits for this head's bulk stores
+    uint32_t stg_phase = 0;
     const uint32_t s_addr = tmem + lane_off + col_s(t);
     const uint32_t o_addr = tmem + lane_off + col_o(t);
     const uint32_t p_addr = tmem + lane_off + col_p(t);
@@ -568,6 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kRopeQ) {
         if (k == 0 && !(ok = rotate_unit(u, 0))) break;
       }
+      // the previous block has left this head's staging tile before the unit starts: every
+      // warp of the head writes the tile again only after this unit's last PV, which waits
+      // for this thread's arrivals
+      if (stg_issuer) bulk_wait_read0();
       int n = u.qb + 1;
       int lim0 = 0;     // paged mode: keys visible to this row, counted from the unit's first key tile
       int j_mask = 0;   // paged mode: first key tile that crosses the last key of some row of this warp
@@ -681,7 +703,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       const int row_tok = u.qb * kTile + r;
       const int tok = seq_start[u.seq] + row_tok;  // checked against T too: cu_seqlens is not trusted
-      if (head_ok && row_tok < seq_len[u.seq] && tok >= 0 && tok < p.total_tokens) {
+      const int tok0 = seq_start[u.seq] + u.qb * kTile;
+      // a whole block of a head (uniform over the head's 128 threads) leaves by one bulk store
+      const bool bulk = !kRopeQ && !p.out_f32 && head_ok && (u.qb + 1) * kTile <= seq_len[u.seq] && tok0 >= 0 &&
+                        tok0 + kTile <= p.total_tokens;
+      if (bulk) {
+        const float inv = (!kPaged || d > 0.f) ? 1.f / d : 0.f;  // paged: no key and no sink gives 0
+        uint4* rowp = reinterpret_cast<uint4*>(smem + kOffStage + t * kTileBytes + r * 128);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(ob[8 * i + 0]) * inv, __uint_as_float(ob[8 * i + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(ob[8 * i + 2]) * inv, __uint_as_float(ob[8 * i + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(ob[8 * i + 4]) * inv, __uint_as_float(ob[8 * i + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(ob[8 * i + 6]) * inv, __uint_as_float(ob[8 * i + 7]) * inv);
+          rowp[i ^ (r & 7)] = v;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> bulk copy reads
+        mbar_arrive(stg_full + t);
+        if (p.lse) p.lse[(size_t)tok * p.hq + h] = (!kPaged || d > 0.f) ? (m + __log2f(d)) * kLn2 : -INFINITY;
+        if (stg_issuer) {
+          ok = wait_or_abort(stg_full + t, stg_phase, p, abort_flag);
+          stg_phase ^= 1;
+          if (ok) {
+            tma_store_3d(&omap, smem + kOffStage + t * kTileBytes, 0, h, tok0);
+            bulk_commit();
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      } else if (head_ok && row_tok < seq_len[u.seq] && tok >= 0 && tok < p.total_tokens) {
         const float inv = (!kPaged || d > 0.f) ? 1.f / d : 0.f;  // paged: no key and no sink gives 0
         const size_t row = (size_t)tok * p.hq + h;
         if (p.out_f32) {
@@ -708,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- teardown
+  if (warp >= 4 && (warp & 3) == 0 && lane == 0) bulk_wait0();  // bulk stores complete before exit
   tc_fence_before();
   __syncthreads();
   if (warp == kTmemWarp) {
@@ -727,16 +779,17 @@ cudaError_t prefill_configure() {
 }
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const CUtensorMap& omap,
                            const PrefillParams& p, int num_sms, bool paged, cudaStream_t stream) {
   const long long ppg = (p.group + 1) / 2;
   const long long upper = ppg * p.hkv * ((long long)(p.total_tokens + kTile - 1) / kTile + p.batch);
   const int grid = (int)std::min<long long>(std::max(1, num_sms), std::max(1LL, upper));
   if (paged)
-    prefill_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+    prefill_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, omap, p);
   else if (p.inv_freq)
-    prefill_kernel<false, true><<<grid, kThreads, kSmemBytesRope, stream>>>(qmap, kmap, vmap, p);
+    prefill_kernel<false, true><<<grid, kThreads, kSmemBytesRope, stream>>>(qmap, kmap, vmap, omap, p);
   else
-    prefill_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+    prefill_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, omap, p);
   return cudaGetLastError();
 }
 

@@ -45,10 +45,12 @@ cudaError_t prefill_configure();
 
 // Enqueue the persistent prefill kernel: `grid_ctas` <= number of SMs.
 // qmap is a 3-D map over [T, Hq, 64] with boxes of 128 tokens x 1 head x 64
-// dims.  Contiguous mode: kmap / vmap are the same over [T, Hkv, 64].  Paged
+// dims; omap the same over the output (bf16 output only: whole 128-row blocks
+// are written by bulk tensor stores; with fp32 output it is not used).  Contiguous mode: kmap / vmap are the same over [T, Hkv, 64].  Paged
 // mode: 2-D maps over the pools viewed as [num_pages * Hkv * 16, 64] with
 // boxes of one (page, kv head) slab of 16 rows.
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const PrefillParams& p, int num_sms, bool paged, cudaStream_t stream);
+                           const CUtensorMap& omap, const PrefillParams& p, int num_sms, bool paged,
+                           cudaStream_t stream);
 
 }  // namespace sa
