@@ -80,7 +80,10 @@ typedef enum {
  *               tile, are masked and their values zeroed before the product,
  *               so even NaN or Inf there does not reach it.
  *   out         [total_tokens, num_q_heads, head_dim], bf16 or fp32 per
- *               out_dtype.  Written for every token of every sequence.
+ *               out_dtype, 16-byte aligned, not overlapping q, k or v.
+ *               Written for every token of every sequence and nowhere else
+ *               (bf16: a head's 128-row block lying wholly inside its
+ *               sequence goes out as one bulk tensor store).
  *   lse         optional fp32 [total_tokens, num_q_heads] (natural-log
  *               normaliser including the sink); NULL to skip.
  * Limits: batch <= 1024; max_seqlen < 2^24; total_tokens * num_q_heads < 2^31.

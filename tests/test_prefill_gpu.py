@@ -190,3 +190,19 @@ def test_prefill_running_max_moves_often(how):
                                     scale)
     assert_parity(out, want)
     lse_close(lse, want_lse)
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_prefill_writes_only_its_output_rows(out_dtype):
+    """The output may be a view into a larger buffer: whole 128-row bf16 blocks
+    leave by bulk tensor store (bounded by the view's T rows), partial blocks and
+    fp32 rows by direct stores; rows before and after the view stay as they were."""
+    lens = [384, 200, 256]  # whole blocks, a partial last block, whole blocks again
+    inp = workloads.make_prefill(lens, num_q_heads=16, num_kv_heads=2, seed=33, sink_mode="mixed", device="cuda")
+    T, H = inp.total_tokens, inp.num_q_heads
+    big = torch.full((T + 320, H, 64), float("nan"), dtype=out_dtype, device="cuda")
+    out = big[64:64 + T]  # starts 64 rows into the allocation
+    sa.sink_attn_prefill(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, inp.scale, out=out, max_seqlen=inp.max_seqlen)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[:64].float()).all() and torch.isnan(big[64 + T:].float()).all()
+    want, _ = full_oracle(inp)
+    assert_parity(out, want, bf16_output=out_dtype == torch.bfloat16)
