@@ -12,10 +12,16 @@
 //     for two 128x128 score tiles.  Units are ordered by sequence (longest
 //     first) and within a sequence by query block (most key tiles first), the
 //     heads of one group adjacent, so that concurrently running CTAs read the
-//     same K/V from L2; they are dealt to CTAs in a serpentine order.
-//   * warp 2 (elected lane): TMA producer.  Loads the two 128x64 Q tiles of a
-//     unit, then K_0, V_0, K_1, V_1, ... through an 8-slot ring of 16 KiB
-//     tiles (128-byte swizzle), each slot guarded by a full/empty mbarrier.
+//     same K/V from L2.  A CTA takes its next unit from a launch-wide counter
+//     (a unit of schedule order at a time), so CTAs on slower SMs take fewer:
+//     with a fixed serpentine deal the last CTA ended ~22 us after the first
+//     on the 8192-token workload (some SMs run ~2 % slower throughout).
+//     Launches captured into a graph keep the serpentine deal.
+//   * warp 2 (elected lane): TMA producer.  Takes the CTA's units and publishes
+//     each, one unit ahead, in a shared-memory ring every role reads; loads the
+//     two 128x64 Q tiles of a unit, then K_0, V_0, K_1, V_1, ... through an
+//     8-slot ring of 16 KiB tiles (128-byte swizzle), each slot guarded by a
+//     full/empty mbarrier.
 //   * warps 1 and 3: MMA issuers for head 0 and head 1.  S_t = Q_t K_j^T
 //     (M=128, N=128, K=64) into TMEM, and O_t += P_t V_j (M=128, N=64, K=128)
 //     with P_t read from TMEM (A operand) and V_j from shared memory (MN-major
@@ -63,8 +69,16 @@
 #include "tcgen05.cuh"
 
 #include <algorithm>
+#include <atomic>
 
 namespace sa {
+
+// Unit counters for the dynamic deal: slot s holds {units handed out, CTAs
+// finished}, and the last CTA of a launch zeroes it again.  Launches take the
+// slots in turn, so two launches share one only if they run at the same time
+// kSchedSlots launches apart.
+constexpr int kSchedSlots = 1 << 16;
+__device__ unsigned g_prefill_sched[kSchedSlots][2];
 
 namespace {
 
@@ -88,9 +102,11 @@ constexpr float kRescaleThreshold = 8.f;
 constexpr int kOffQ = 0;                                // 2 Q tiles
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;         // kSlots K/V tiles
 constexpr int kOffBar = kOffRing + kSlots * kTileBytes;  // mbarriers
-constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 + 2;
-constexpr int kOffMisc = kOffBar + 256;
-constexpr int kOffSeq = kOffMisc + 64;
+constexpr int kUnitRing = 16;  // units published by the producer, read by every role
+constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 2 + 2 + kUnitRing;
+constexpr int kBarBytes = 384;
+constexpr int kOffMisc = kOffBar + kBarBytes;
+constexpr int kOffSeq = kOffMisc + 64 + 4 * kUnitRing;
 constexpr int kSeqArrays = 6;
 // bf16 output of a whole 128-row block leaves through a staging tile per head
 // (the Q tile's layout: 128-byte swizzle) and one bulk tensor store
@@ -106,7 +122,7 @@ constexpr int kSmemBytesRope = kOffRopeTurn + 32 * 8 + 1024;
 static_assert(kSmemBytesRope <= 227 * 1024, "shared memory of the rotary mode");
 constexpr int kPage = 16;
 constexpr int kSlabBytes = kPage * kD * 2;  // one (page, kv head) slab: 2 KiB
-static_assert(kNumBars * 8 <= 256, "barrier area");
+static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
 
 struct Bars {
   uint64_t* q_full;
@@ -155,16 +171,19 @@ struct Unit {
   int pair; // pair of query heads within the group
 };
 
-__device__ __forceinline__ bool next_unit(int k, int total, int pairs_per_group, int hkv, Cursor& cur, Unit& u) {
-  const int c = blockIdx.x, G = gridDim.x;
-  const long long idx = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
-  if (idx >= total) return false;
-  const int ui = (int)idx;
+// Unit index (schedule order) -> unit.  Indices must not decrease between calls.
+__device__ __forceinline__ void decode_unit(int ui, int pairs_per_group, int hkv, Cursor& cur, Unit& u) {
   u.pair = ui % pairs_per_group;
   const int rest = ui / pairs_per_group;
   u.g = rest % hkv;
   u.seq = cur.seek(rest / hkv, u.qb);
-  return true;
+}
+
+// The k-th unit index of this CTA under the static deal (serpentine), or -1.
+__device__ __forceinline__ int static_unit(int k, int total) {
+  const int c = blockIdx.x, G = gridDim.x;
+  const long long idx = (long long)k * G + ((k & 1) ? (G - 1 - c) : c);
+  return idx < total ? (int)idx : -1;
 }
 
 // Paged mode: keys a unit needs, [0, kend): up to the position of its last
@@ -253,6 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   bars.drain = bars.o_done + 2;
   bars.q_ready = bars.drain + 1;
   uint64_t* stg_full = bars.q_ready + 2;  // [2] softmax rows of a block written to the staging tile
+  uint64_t* unit_ready = stg_full + 2;    // [kUnitRing] producer -> all: unit k published in unit_ring[k % kUnitRing]
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + kOffMisc + 64);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* total_qblocks = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -295,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bars.q_ready + 1, 128);
     mbar_init(stg_full, 128);
     mbar_init(stg_full + 1, 128);
+    for (int i = 0; i < kUnitRing; ++i) mbar_init(unit_ready + i, 1);
     *abort_flag = 0;
     *zeroed_count = 0;
     fence_barrier_init();
@@ -338,6 +360,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_units = (int)min(total_ll, (long long)0x7fffffff);
   Cursor cur;
   cur.init(seq_nqb, B);
+  // Unit k of this CTA (every role reads it from the ring): 1 got one, 0 none left, -1 aborted.
+  auto unit_at = [&](int k, Unit& v) -> int {
+    if (!__all_sync(0xffffffffu, wait_or_abort(unit_ready + (k % kUnitRing), (k / kUnitRing) & 1, p, abort_flag)))
+      return -1;
+    const int idx = unit_ring[k % kUnitRing];
+    if (idx < 0) return 0;
+    decode_unit(idx, pairs_per_group, p.hkv, cur, v);
+    return 1;
+  };
 
   uint8_t* q_tile[2] = {smem + kOffQ, smem + kOffQ + kTileBytes};
   uint8_t* ring = smem + kOffRing;
@@ -354,7 +385,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ring_i = 0;
     Unit u;
     bool ok = true;
-    for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+    // The CTA's k-th unit: the next one of the launch (dynamic deal) or the static one,
+    // published to every role one unit ahead (so the MMA warps know the next unit while
+    // they work on this one).
+    auto publish = [&](int kk) -> int {
+      int v = 0;
+      if (lane == 0) {
+        if (p.sched_slot >= 0) {
+          v = (int)atomicAdd(&g_prefill_sched[p.sched_slot][0], 1u);
+          if (v >= total_units) v = -1;
+        } else {
+          v = static_unit(kk, total_units);
+        }
+        unit_ring[kk % kUnitRing] = v;
+        mbar_arrive(unit_ready + (kk % kUnitRing));  // release: the ring entry is visible to its waiters
+      }
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    int idx_next = publish(0);
+    for (int k = 0; ok; ++k) {
+      const int idx = idx_next;
+      if (idx < 0) break;
+      idx_next = publish(k + 1);
+      decode_unit(idx, pairs_per_group, p.hkv, cur, u);
       if (k > 0 && !(ok = __all_sync(0xffffffffu, wait_or_abort(bars.q_empty, (k - 1) & 1, p, abort_flag)))) break;
       const int t0 = seq_start[u.seq] + u.qb * kTile;
       const int hA = u.g * p.group + 2 * u.pair;
@@ -449,9 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t), a_p = tmem + col_p(t);
     int zeroings = 0;  // tail-V zeroings met so far
     Unit u, un;
-    bool ok = true;
-    bool have = next_unit(0, total_units, pairs_per_group, p.hkv, cur, u), have_next = false;
-    for (int k = 0; ok && have; ++k, u = un, have = have_next) {
+    int got = unit_at(0, u), got_next = 0;
+    bool ok = got >= 0;
+    for (int k = 0; ok && got > 0; ++k, u = un, got = got_next) {
       int n = u.qb + 1, kend = 0;
       if constexpr (kPaged) {
         kend = paged_kend(seq_kv[u.seq], seq_len[u.seq], u.qb);
@@ -475,8 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(bars.slot_empty + ring_i % kSlots);
         if (n == 1) umma_commit(bars.q_empty);
       }
-      // the next unit, worked out here, where the warp has only waits ahead of it
-      have_next = next_unit(k + 1, total_units, pairs_per_group, p.hkv, cur, un);
+      // the next unit (published before this unit's Q tiles were loaded), read here, where
+      // the warp has only waits ahead of it
+      got_next = unit_at(k + 1, un);
+      if (!(ok = got_next >= 0)) break;
       ++ring_i;
       // keys of the unit's last tile it needs (only the last tile can end early)
       const int valid_last = (kPaged ? kend : seq_len[u.seq]) - (n - 1) * kTile;
@@ -582,7 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     Unit u;
     bool ok = true;
-    for (int k = 0; ok && next_unit(k, total_units, pairs_per_group, p.hkv, cur, u); ++k) {
+    int got = 0;
+    for (int k = 0; ok && (got = unit_at(k, u)) > 0; ++k) {
       if constexpr (kRopeQ) {
         if (k == 0 && !(ok = rotate_unit(u, 0))) break;
       }
@@ -690,7 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this unit's last PV runs; kept out of the tile loop, whose every iteration ran
         // slower with it inside
         Unit un;
-        if (next_unit(k + 1, total_units, pairs_per_group, p.hkv, cur, un) && !(ok = rotate_unit(un, k + 1))) break;
+        const int got_next = unit_at(k + 1, un);
+        if (!(ok = got_next >= 0) || (got_next > 0 && !(ok = rotate_unit(un, k + 1)))) break;
       }
       // ---- epilogue: wait for the last PV, normalise, store
       ok = wait_or_abort(bars.o_done + t, oph, p, abort_flag);
@@ -762,6 +819,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 4 && (warp & 3) == 0 && lane == 0) bulk_wait0();  // bulk stores complete before exit
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && p.sched_slot >= 0) {
+    // the last CTA of the launch zeroes its counters for the next launch (every unit
+    // fetch of every CTA precedes its count here)
+    __threadfence();
+    if (atomicAdd(&g_prefill_sched[p.sched_slot][1], 1u) == gridDim.x - 1) {
+      g_prefill_sched[p.sched_slot][0] = 0;
+      g_prefill_sched[p.sched_slot][1] = 0;
+      __threadfence();
+    }
+  }
   if (warp == kTmemWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -778,9 +845,21 @@ cudaError_t prefill_configure() {
                               kSmemBytesRope);
 }
 
+// Counter slot of a launch, or -1 for the static deal: a launch captured into a
+// graph keeps the static deal, since every replay of the graph (and every
+// instance made from it) would share the one slot baked into it.
+static int prefill_sched_slot(cudaStream_t stream) {
+  static std::atomic<unsigned> next{0};
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return -1;
+  return (int)(next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
+}
+
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const CUtensorMap& omap,
-                           const PrefillParams& p, int num_sms, bool paged, cudaStream_t stream) {
+                           const CUtensorMap& omap, const PrefillParams& params, int num_sms, bool paged,
+                           cudaStream_t stream) {
+  PrefillParams p = params;
+  p.sched_slot = prefill_sched_slot(stream);
   const long long ppg = (p.group + 1) / 2;
   const long long upper = ppg * p.hkv * ((long long)(p.total_tokens + kTile - 1) / kTile + p.batch);
   const int grid = (int)std::min<long long>(std::max(1, num_sms), std::max(1LL, upper));

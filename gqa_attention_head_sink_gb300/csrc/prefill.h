@@ -25,6 +25,10 @@ struct PrefillParams {
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
   int withhold_copies;  // failure-path test: the producer issues no copies, so the waits time out
+  // Work distribution: the slot of the per-device unit counters this launch
+  // takes its units from (one at a time, in schedule order: longest first), or
+  // -1 for the static deal (captured launches).  Set by launch_prefill.
+  int sched_slot;
   // Paged mode (chunked prefill against the paged KV cache): the keys of
   // sequence b are its kv_len[b] cached tokens, read page by page, and its
   // n_b query rows are the last n_b of them (row i at position

@@ -206,3 +206,21 @@ def test_prefill_writes_only_its_output_rows(out_dtype):
     assert torch.isnan(big[:64].float()).all() and torch.isnan(big[64 + T:].float()).all()
     want, _ = full_oracle(inp)
     assert_parity(out, want, bf16_output=out_dtype == torch.bfloat16)
+
+def test_prefill_concurrent_launches_on_several_streams():
+    """Launches running at the same time on different streams each take their
+    units from their own counter: every output equals the one of a lone launch,
+    bit for bit (the work split between CTAs does not change any result)."""
+    inp = workloads.make_prefill([640, 384, 1000, 257], num_q_heads=16, num_kv_heads=2, seed=41, sink_mode="mixed",
+                                 device="cuda")
+    ref, _ = run(inp, out_dtype=torch.bfloat16)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    outs = [torch.empty_like(ref) for _ in range(len(streams) * 4)]
+    torch.cuda.synchronize()
+    for i, out in enumerate(outs):
+        with torch.cuda.stream(streams[i % len(streams)]):
+            sa.sink_attn_prefill(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, inp.scale, out=out,
+                                 max_seqlen=inp.max_seqlen)
+    torch.cuda.synchronize()
+    for out in outs:
+        assert torch.equal(out, ref)
