@@ -24,6 +24,10 @@ queries, outputs, page-table entries); `roofline` for the prefill kernel
 GPU pool; `e2e` = the same through host buffers with the copies timed;
 `cpu_baseline` = the float64 oracle timed on a bounded sample on this host.
 
+`--sweep` instead prints one JSON line per shape: the prefill over single
+sequences of 1K..128K tokens and packed batches, the decode over batch sizes
+and cache lengths (default splits), each timed per call with L2 flushed.
+
 `--impl reference` times the float64 CPU oracle (the only implementation the
 method's source provides a definition for) on bounded samples of the same
 workload and prints the same line with "impl": "reference".
@@ -714,13 +718,68 @@ def run_reference(args, dist, rank, world):
     }
 
 
+def run_sweep(args):
+    """Prefill TFLOP/s and decode GB/s across shapes (gpt-oss heads: 64 query,
+    8 kv, head_dim 64), each shape timed per call (median of `args.steps`
+    calls after `args.warmup`), L2 flushed between calls outside the events."""
+    import statistics
+    import torch
+    import gqa_attention_head_sink_gb300 as sa
+    from gqa_attention_head_sink_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sa.load()
+    peaks, _ = _peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    steps, warm = max(5, min(args.steps, 50)), max(3, args.warmup)
+
+    def timed(call):
+        for _ in range(warm):
+            call()
+        ts = []
+        for i in range(steps):
+            flush.fill_(float(i))
+            a, b = _events()
+            a.record()
+            call()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    prefill_shapes = [[n] for n in (1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)]
+    prefill_shapes += [[4096] * 8, [1024] * 32, [512] * 64]
+    for lens in prefill_shapes:
+        inp = workloads.make_prefill(lens, seed=11, device=dev)
+        out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=dev)
+        ms = timed(lambda: sa.sink_attn_prefill(inp.q, inp.k, inp.v, inp.sinks, inp.cu_seqlens, inp.scale, out=out,
+                                                max_seqlen=inp.max_seqlen))
+        tf = workloads.prefill_flops(lens, inp.num_q_heads) / (ms * 1e-3) / 1e12
+        print(json.dumps({"sweep": "prefill", "seqlens": f"{len(lens)} x {lens[0]}", "ms": round(ms, 4),
+                          "TFLOP/s": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4)}), flush=True)
+        del inp, out
+    for batch, L in [(1, 8192), (8, 8192), (64, 1024), (64, 8192), (256, 8192), (16, 32768), (128, 32768)]:
+        dec = workloads.make_decode([L] * batch, seed=12, device=dev)
+        out = torch.empty(dec.q.shape, dtype=torch.bfloat16, device=dev)
+        ms = timed(lambda: sa.sink_attn_decode(dec.q, dec.k_pages, dec.v_pages, dec.page_table, dec.seqlens_t,
+                                               dec.sinks, dec.scale, out=out, max_seqlen=dec.max_seqlen))
+        gbs = workloads.decode_bytes(dec.seqlens, dec.num_q_heads, dec.num_kv_heads, out_bytes=2) / (ms * 1e-3) / 1e9
+        print(json.dumps({"sweep": "decode", "batch": batch, "cached": L, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                          "frac": round(gbs / peaks["hbm_gbs"], 4)}), flush=True)
+        del dec, out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true", help="one line per prefill / decode shape instead")
     args = ap.parse_args(argv)
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
