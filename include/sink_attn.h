@@ -35,6 +35,11 @@
  *     outside the contract.
  *   - Device-side waits are bounded; a wait that gives up records a timeout
  *     that sink_attn_get_device_error() reports.
+ *   - The prefill kernels hand work units to their CTAs at run time from one
+ *     of 65,536 per-device counter slots, taken in turn by successive launches
+ *     (calls may run concurrently on different streams); a launch captured
+ *     into a CUDA graph uses a fixed deal instead.  Results do not depend on
+ *     the deal.
  */
 #ifndef SINK_ATTN_H_
 #define SINK_ATTN_H_
