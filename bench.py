@@ -613,14 +613,15 @@ def _cores():
 
 
 PREFILL_SAMPLE_HEADS = 16  # two kv groups of the 8192-token sequence
+REFERENCE_BUDGET_S = 150.0  # the reference arm's whole timed run (warm-up + steps), about
 
 
-def _oracle_prefill_sample(pre):
-    """Time the oracle on the first PREFILL_SAMPLE_HEADS query heads (their kv
+def _oracle_prefill_sample(pre, nh=PREFILL_SAMPLE_HEADS):
+    """Time the oracle on the first `nh` query heads (a power of two: their kv
     heads) of the full 8192-token sequence; returns (seconds, flops)."""
     import oracle
-    nh = PREFILL_SAMPLE_HEADS
-    nkv = nh // (pre.num_q_heads // pre.num_kv_heads)
+    group = pre.num_q_heads // pre.num_kv_heads
+    nkv = max(1, nh // group)
     q, k, v = pre.q[:, :nh].cpu(), pre.k[:, :nkv].cpu(), pre.v[:, :nkv].cpu()
     t0 = time.perf_counter()
     oracle.prefill(q, k, v, pre.sinks[:nh].cpu(), pre.cu_seqlens.cpu(), pre.scale)
@@ -682,16 +683,27 @@ def run_reference(args, dist, rank, world):
     if rank != 0:
         return None
     pre = workloads.workload(PREFILL, device="cpu")
-    dec = workloads.make_decode([8192] * 8, seed=2, sink_mode="normal2", scale=0.125, num_splits=8)
-    steps = args.steps if args.steps <= 3 else 3  # each step is seconds of float64 work
-    warm = min(args.warmup, 1)
+    dec = workloads.make_decode([8192] * 16, seed=2, sink_mode="normal2", scale=0.125, num_splits=8)
+    # Exactly the requested steps and warm-up; each step is a sample of the workload sized
+    # so the whole run stays within a few minutes: the first nh query heads of the prefill
+    # (a power of two) and the first ns (<= 16) of its 8192-token decode sequences, from one
+    # timed head and sequence.
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    per_step = min(4.0, REFERENCE_BUDGET_S / (steps + warm))
+    t_head, _ = _oracle_prefill_sample(pre, 1)
+    t_seq, _ = _oracle_decode_sample(dec, 1)
+    nh = 1
+    while nh < pre.num_q_heads and 2 * nh * t_head <= 0.85 * per_step:
+        nh *= 2
+    ns = max(1, min(dec.batch, int(0.15 * per_step / max(t_seq, 1e-9))))
     for _ in range(warm):
-        _oracle_prefill_sample(pre)
+        _oracle_prefill_sample(pre, nh)
+        _oracle_decode_sample(dec, ns)
     tp, td, flops, dbytes = 0.0, 0.0, 0, 0
     for _ in range(steps):
-        dt, flops = _oracle_prefill_sample(pre)
+        dt, flops = _oracle_prefill_sample(pre, nh)
         tp += dt
-        ddt, dbytes = _oracle_decode_sample(dec)
+        ddt, dbytes = _oracle_decode_sample(dec, ns)
         td += ddt
     val = flops * steps / tp / 1e12
     return {
@@ -711,8 +723,8 @@ def run_reference(args, dist, rank, world):
         "config": _config(world),
         "decode": {"value": round(dbytes * steps / td / 1e9, 4), "unit": "GB/s"},
         "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
-                         "sample": f"{PREFILL_SAMPLE_HEADS}/64 query heads of the 8192-token prefill and 8 of the 64 "
-                                   "decode sequences per step"},
+                         "sample": f"{nh}/64 query heads of the 8192-token prefill and {ns} of the 64 decode "
+                                   "sequences (8192 tokens each) per step"},
         "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
