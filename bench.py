@@ -491,8 +491,9 @@ def _next_rows(sa, dev, stream, flush, peaks, peak_src):
         "separate": {"value": round(fl / (ms_sep * 1e-3) / 1e12, 3), "ms": round(ms_sep, 4),
                      "kernels": "qkv_rope_kernel (q, k and v) + prefill_kernel"},
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(tf / peaks["bf16_tflops"], 4), "traffic": None,
-                     "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
+                     "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "traffic": _traffic("prefill_kernel/rope_prefill", PREFILL_SOURCES),
+                     "kernel": "prefill_kernel (rotary mode)", "peak_source": f"{peak_src} (cuBLAS bf16 burst)"}}
     del ro, pristine, out
     torch.cuda.empty_cache()
     return res

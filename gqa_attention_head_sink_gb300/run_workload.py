@@ -6,7 +6,9 @@ Meant for profiling one kernel on one workload (e.g. under ncu with -k and
 -c), so that the profiled process holds only that workload's tensors on the
 device, not the whole benchmark.  Workloads are those of workloads.py:
 tiny_prefill, gptoss_prefill, ragged_prefill, decode, long_decode,
-mtp_decode (--q-len new tokens per sequence), chunked_prefill, qkv_rope.
+mtp_decode (--q-len new tokens per sequence), chunked_prefill, qkv_rope, and
+rope_prefill (the 8192 raw projections of qkv_rope through the rotary-mode
+prefill, k and v rotated once beforehand).
 Outputs are bf16.  Prints the mean device time per call (CUDA events; not a
 benchmark figure: no L2 flush, few calls).
 """
@@ -52,6 +54,16 @@ def _call(name: str, dev, q_len: int):
         f, af = sa.sink_attn_yarn_inv_freq(64, **workloads.YARN_SETTINGS)
         f = f.to(dev)
         return lambda: sa.sink_attn_qkv_rope(w.q, w.k, w.v, w.positions, f, af, w.q_bias, w.k_bias, w.v_bias)
+    if name == "rope_prefill":
+        w = workloads.make_qkv_rope(8192, device=dev)
+        f, af = sa.sink_attn_yarn_inv_freq(64, **workloads.YARN_SETTINGS)
+        f = f.to(dev)
+        sa.sink_attn_qkv_rope(None, w.k, w.v, w.positions, f, af, None, w.k_bias, w.v_bias)
+        sinks = (2.0 * torch.randn(64, generator=torch.Generator(device=dev).manual_seed(1), device=dev)).float()
+        cu = torch.tensor([0, 8192], dtype=torch.int32, device=dev)
+        out = torch.empty(w.q.shape, dtype=torch.bfloat16, device=dev)
+        return lambda: sa.sink_attn_prefill_rope(w.q, w.k, w.v, sinks, cu, 0.125, f, af, q_bias=w.q_bias, out=out,
+                                                 max_seqlen=8192)
     raise SystemExit(f"unknown workload {name!r}")
 
 
