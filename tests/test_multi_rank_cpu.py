@@ -79,3 +79,39 @@ def test_traffic_is_reported_only_for_the_captured_source():
             continue
         name, digest, nbytes = line.split()[:3]
         assert len(digest) == 16 and float(nbytes) > 0
+
+
+def test_reference_arm_runs_the_requested_steps(monkeypatch):
+    # the reference arm times exactly --steps / --warmup steps, each a sample sized from one
+    # timed head and one timed sequence (fakes stand in for the float64 oracle here)
+    import argparse
+    import bench
+    calls = {"pre": [], "dec": []}
+
+    def fake_pre(pre, nh=bench.PREFILL_SAMPLE_HEADS):
+        calls["pre"].append(nh)
+        return 0.05 * nh, 1000 * nh
+
+    def fake_dec(dec, seqs=8):
+        calls["dec"].append(seqs)
+        return 0.01 * seqs, 100 * seqs
+
+    monkeypatch.setattr(bench, "_oracle_prefill_sample", fake_pre)
+    monkeypatch.setattr(bench, "_oracle_decode_sample", fake_dec)
+    monkeypatch.setattr(bench.workloads, "workload", lambda name, device="cpu": argparse.Namespace(num_q_heads=64))
+    monkeypatch.setattr(bench.workloads, "make_decode", lambda *a, **k: argparse.Namespace(batch=16))
+    for steps, warm in [(20, 3), (1000, 10), (1, 0)]:
+        calls["pre"].clear()
+        calls["dec"].clear()
+        line = bench.run_reference(argparse.Namespace(steps=steps, warmup=warm), None, 0, 1)
+        assert line["steps"] == steps and line["warmup"] == warm
+        # one calibration call each, then warm-up + steps samples of one size
+        assert calls["pre"][0] == 1 and calls["dec"][0] == 1
+        nh, ns = calls["pre"][-1], calls["dec"][-1]
+        assert len(calls["pre"]) == 1 + warm + steps and set(calls["pre"][1:]) == {nh}
+        assert len(calls["dec"]) == 1 + warm + steps and set(calls["dec"][1:]) == {ns}
+        assert nh & (nh - 1) == 0 and 1 <= nh <= 64 and 1 <= ns <= 16
+        per_step = min(4.0, bench.REFERENCE_BUDGET_S / (steps + warm))
+        assert nh == 1 or 0.05 * nh <= 0.85 * per_step
+        assert line["value"] == round(1000 * nh * steps / (0.05 * nh * steps) / 1e12, 6)
+    assert bench.run_reference(argparse.Namespace(steps=3, warmup=1), None, 1, 2) is None  # other ranks: no work
